@@ -1,0 +1,463 @@
+"""Benchmark of the multi-head attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+One step is one whole forward pass (the error-word reset, the QKV projection
+with head split, the fused attention kernel and the output projection) over
+one batch of seeded synthetic inputs already resident in HBM. L2 is flushed
+(a 512 MiB device write) between timed steps, outside the timed events. With
+N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(replicas only: the forward pass has no exchange step), the time is the max
+over ranks and the value counts the work of all ranks.
+
+Prints one JSON line. Counting: attention core 4 * n_q * n_k * d_h per (batch
+item, head), halved under a causal mask; projections 2 * rows * d_in * width.
+With a padding mask the effective count (valid rows and keys) is reported.
+
+--impl reference times the oracle (plain fp64 numpy on the host cores) on a
+bounded sample of the same workload: one (batch item, head) unit per step.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MHA forward TFLOP/s and fraction of GB300 bf16 dense peak, 1 GPU"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1,
+                    help="workload index (0..4); the JSON line is for this one")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the per-workload table of the other bf16 workloads")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup(n):
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def stored_traffic(kernel, workload_name):
+    """Per-launch DRAM bytes from a committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))[kernel][workload_name]
+    except Exception:
+        return None
+    src = os.path.join(ROOT, "head_scaled_dot_gb300", "csrc", d["source"])
+    if not os.path.exists(src) or source_hash(src) != d["source_sha256_16"]:
+        return None
+    return d["dram_bytes_per_launch"]
+
+
+def to_device(inp, dev):
+    import torch
+    return {k: (v.to(dev) if torch.is_tensor(v) and k != "valid_len" else v)
+            for k, v in inp.items()}
+
+
+def measure_workload(w, steps, warmup, dev, world, e2e=True):
+    """Times `steps` forward passes of workload w. Returns a dict of results."""
+    import torch
+
+    from head_scaled_dot_gb300 import mha, workcount, workloads
+
+    inp = workloads.make_inputs(w)
+    lens = None if inp["valid_len"] is None else [int(x) for x in inp["valid_len"]]
+    t = to_device(inp, dev)
+    lib = mha.load()
+    B, n_q, n_k = w.B, w.n_q, w.n_k
+    dt = workloads.torch_dtype(w.dtype)
+    nbytes = mha.workspace_size(B, n_q, n_k, w.d_model, w.h, w.d_h, w.d_vh, w.d_o, w.dtype)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    Y = torch.empty((B, n_q, w.d_o), dtype=dt, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = mha._stream(stream)
+    import ctypes
+    P = ctypes.c_void_p
+    L = mha.workspace_layout(B, n_q, n_k, w.h, w.d_h, w.d_vh, w.dtype)
+    base = ws.data_ptr()
+    err, Qp, Kp, Vp, Zp = base, base + L["q"], base + L["k"], base + L["v"], base + L["z"]
+    lens_arg, keep = mha._lens(lens, B)
+    DT, MK = mha.DTYPES[w.dtype], mha.MASKS[w.mask]
+    X_kv_p = None if t["X_kv"] is None else P(t["X_kv"].data_ptr())
+
+    def step(ev):
+        # the three kernels mha_forward enqueues (it also resets the 4-byte
+        # error word first), with events between them
+        ev[0].record(stream)
+        rc = lib.mha_qkv_projection(P(t["X_q"].data_ptr()), X_kv_p, P(t["W_Q"].data_ptr()),
+                                    P(t["W_K"].data_ptr()), P(t["W_V"].data_ptr()), P(Qp), P(Kp),
+                                    P(Vp), B, n_q, n_k, w.d_model, w.h, w.d_h, w.d_vh, DT,
+                                    P(err), sp)
+        ev[1].record(stream)
+        rc |= lib.mha_attention(P(Qp), P(Kp), P(Vp), P(Zp), B, n_q, n_k, w.h, w.d_h, w.d_vh,
+                                float(w.c), MK, lens_arg, 0 if w.cross else 1, DT, P(err), sp)
+        ev[2].record(stream)
+        rc |= lib.mha_output_projection(P(Zp), P(t["W_O"].data_ptr()), P(Y.data_ptr()), B, n_q,
+                                        w.h, w.d_vh, w.d_o, DT, P(err), sp)
+        ev[3].record(stream)
+        if rc != 0:
+            raise RuntimeError("launch failed with status %d" % rc)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    torch.cuda.synchronize(dev)
+    ws[:4].zero_()
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        step(mk())
+    torch.cuda.synchronize(dev)
+    events = [mk() for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    launches0 = mha.launch_count()
+    for ev in events:
+        flush.fill_(1.0)  # L2 flush, outside the timed events
+        step(ev)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    launches = mha.launch_count() - launches0
+    clk = clocks.stop()
+    status = mha.get_device_error(P(err), stream)
+    if status != 0:
+        raise RuntimeError("device error word: %d" % status)
+    per = {"qkv": [], "attention": [], "out": [], "step": []}
+    for ev in events:
+        per["qkv"].append(ev[0].elapsed_time(ev[1]))
+        per["attention"].append(ev[1].elapsed_time(ev[2]))
+        per["out"].append(ev[2].elapsed_time(ev[3]))
+        per["step"].append(ev[0].elapsed_time(ev[3]))
+    total_ms = sum(per["step"])
+    fl = workcount.flops(w, lens)
+    res = {"inputs": inp, "lens": lens, "flops": fl, "total_ms": total_ms, "per": per,
+           "launches": launches, "clocks": clk, "Y": Y, "ws": ws}
+
+    if e2e:
+        res["e2e"] = measure_e2e(w, inp, t, steps, warmup, dev, world, ws, flush)
+    return res
+
+
+def measure_e2e(w, inp, t, steps, warmup, dev, world, ws, flush):
+    """The public call (mha.forward) with pinned host inputs copied in and the
+    result copied out inside the timed region of every step."""
+    import torch
+
+    from head_scaled_dot_gb300 import mha
+    hX = inp["X_q"].pin_memory()
+    hXkv = None if inp["X_kv"] is None else inp["X_kv"].pin_memory()
+    dX = torch.empty_like(t["X_q"])
+    dXkv = None if hXkv is None else torch.empty_like(t["X_kv"])
+    Y = torch.empty((w.B, w.n_q, w.d_o), dtype=t["X_q"].dtype, device=dev)
+    hY = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def one(ev0, ev1):
+        ev0.record(stream)
+        dX.copy_(hX, non_blocking=True)
+        if dXkv is not None:
+            dXkv.copy_(hXkv, non_blocking=True)
+        mha.forward(dX, dXkv, t["W_Q"], t["W_K"], t["W_V"], t["W_O"], w.h, w.d_h, w.d_vh, w.c,
+                    w.mask, inp["valid_len"], out=Y, workspace=ws, check=False)
+        hY.copy_(Y, non_blocking=True)
+        ev1.record(stream)
+        ev1.synchronize()  # the caller reads the result on the host
+
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        one(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    barrier(world)
+    tot = 0.0
+    for _ in range(steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        one(e0, e1)
+        tot += e0.elapsed_time(e1)
+    barrier(world)
+    h2d = hX.numel() * hX.element_size() + (0 if hXkv is None else hXkv.numel() * hXkv.element_size())
+    d2h = hY.numel() * hY.element_size()
+    return {"ms": tot, "h2d": h2d, "d2h": d2h}
+
+
+def oracle_sample(w, inp, lens, unit):
+    """Runs the oracle as it stands on one (batch item, head) unit of the
+    workload: the head's projections, its dense attention and its share of
+    the output projection. Returns (seconds, flops)."""
+    import oracle
+    from head_scaled_dot_gb300 import workcount
+    b, i = unit
+    f = lambda x: None if x is None else x.double().numpy()
+    X_q = f(inp["X_q"][b:b + 1])
+    X_kv = None if inp["X_kv"] is None else f(inp["X_kv"][b:b + 1])
+    cq = slice(i * w.d_h, (i + 1) * w.d_h)
+    cv = slice(i * w.d_vh, (i + 1) * w.d_vh)
+    L = None if lens is None else [lens[b]]
+    t0 = time.perf_counter()
+    oracle.mha_forward(X_q, X_kv, f(inp["W_Q"][:, cq]), f(inp["W_K"][:, cq]),
+                       f(inp["W_V"][:, cv]), f(inp["W_O"][cv, :]), 1, w.d_h, w.d_vh, w.c,
+                       oracle.MASK_NAMES[w.mask], L)
+    dt = time.perf_counter() - t0
+    fl = workcount.flops(w.with_(B=1, h=1), L)["total"]
+    return dt, fl
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+def cpu_baseline(w, inp, lens, budget_s=12.0):
+    units = [(b, i) for b in range(w.B) for i in range(w.h)]
+    secs = fl = 0.0
+    done = 0
+    for u in units:
+        dt, f = oracle_sample(w, inp, lens, u)
+        secs += dt
+        fl += f
+        done += 1
+        if secs >= budget_s:
+            break
+    return {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d (batch item, head) units of %s, fp64 numpy, %.1f s"
+                      % (done, len(units), w.name, secs)}
+
+
+def run_reference(args):
+    import torch
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    from head_scaled_dot_gb300 import workloads
+    w = workloads.WORKLOADS[args.config]
+    inp = workloads.make_inputs(w)
+    lens = None if inp["valid_len"] is None else [int(x) for x in inp["valid_len"]]
+    units = [(b, i) for b in range(w.B) for i in range(w.h)]
+    for k in range(args.warmup):
+        oracle_sample(w, inp, lens, units[k % len(units)])
+    secs = fl = 0.0
+    for k in range(args.steps):
+        dt, f = oracle_sample(w, inp, lens, units[k % len(units)])
+        secs += dt
+        fl += f
+    value = fl / secs / 1e12
+    cores = blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "step": "one (batch item, head) unit per step"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "one (batch item, head) unit of %s per step, %d steps"
+                                       % (w.name, args.steps)},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def kernel_rows(res, pk):
+    fl = res["flops"]
+    n = len(res["per"]["step"])
+    rows = {}
+    for name, key in (("qkv_projection", "qkv"), ("attention", "attention"),
+                      ("output_projection", "out")):
+        ms = sum(res["per"][key]) / n
+        tf = fl[key] / (ms * 1e-3) / 1e12
+        rows[name] = {"ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"]}
+    return rows
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from head_scaled_dot_gb300 import mha, workloads
+    mha.load()
+    pk, pk_kind = peaks()
+    w = workloads.WORKLOADS[args.config]
+    res = measure_workload(w, args.steps, args.warmup, dev, world, e2e=not args.no_e2e)
+    total_ms = max_over_ranks(res["total_ms"], world, dev)
+    fl = res["flops"]["total"]
+    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
+    krows = kernel_rows(res, pk)
+    dom = max(krows, key=lambda k: krows[k]["ms"])
+    kernel_file = {"attention": "attn_tc.cu", "qkv_projection": "gemm_tc.cu",
+                   "output_projection": "gemm_tc.cu"}[dom]
+    ach = krows[dom]["tflops"]
+    roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "peak_kind": pk_kind + " burst",
+            "traffic": stored_traffic(dom, w.name)}
+    if w.dtype == "f32":
+        roof["bound"] = "alu"
+    others = {}
+    if not args.no_others and rank == 0:
+        for j, wj in enumerate(workloads.WORKLOADS):
+            if j == args.config or wj.dtype != "bf16":
+                continue
+            r = measure_workload(wj, max(3, args.steps // 2), 3, dev, 1, e2e=False)
+            kr = kernel_rows(r, pk)
+            others[wj.name] = {"tflops": r["flops"]["total"] * len(r["per"]["step"])
+                               / (r["total_ms"] * 1e-3) / 1e12,
+                               "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
+                               "kernels": kr}
+            del r
+    cpu = None
+    if rank == 0:
+        cpu = cpu_baseline(w, res["inputs"], res["lens"])
+    e2e = None
+    if "e2e" in res:
+        e = res["e2e"]
+        e_ms = max_over_ranks(e["ms"], world, dev)
+        e2e = {"value": world * fl * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "n_q": w.n_q, "n_k": w.n_k,
+                   "d_model": w.d_model, "h": w.h, "d_h": w.d_h, "d_vh": w.d_vh, "d_o": w.d_o,
+                   "mask": w.mask, "cross": w.cross, "seed": w.seed,
+                   "valid_len": res["lens"], "l2": "flushed between timed steps (512 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "gflop_per_step": fl / 1e9},
+        "frac_of_bf16_peak": value / world / pk["bf16_tflops"],
+        "roofline": roof,
+        "kernels": krows,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "other_workloads": others,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,76 @@
+// internal.h - host-side interfaces shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mha.h"
+
+namespace mha {
+
+// One GEMM of a grouped launch: out = A (M x K, row-major) * W (K x N,
+// row-major), written through the index map
+//   dest(m, n) = (m / rows_per_group) * s_group_row + (n / cols_per_group) * s_group_col
+//              + (m % rows_per_group) * s_row + (n % cols_per_group)
+// which covers both the plain row-major output (rows_per_group = M,
+// cols_per_group = N, s_row = N) and the head split (B,T,h*d) -> (B,h,T,d)
+// (rows_per_group = T, cols_per_group = d, s_group_row = h*T*d,
+// s_group_col = T*d, s_row = d).
+struct GemmProblem {
+  const void* A;
+  const void* W;
+  void* out;
+  int M, N, K;
+  int rows_per_group, cols_per_group;
+  long long s_group_row, s_group_col, s_row;
+};
+
+static inline GemmProblem plain_problem(const void* A, const void* W, void* out, int M, int N,
+                                        int K) {
+  GemmProblem p{A, W, out, M, N, K, M, N, 0, 0, (long long)N};
+  return p;
+}
+
+static inline GemmProblem head_split_problem(const void* A, const void* W, void* out, int B,
+                                             int T, int h, int d, int K) {
+  GemmProblem p{A,  W, out, B * T, h * d, K, T, d, (long long)h * T * d, (long long)T * d,
+                (long long)d};
+  return p;
+}
+
+// Attention step arguments (Q, K, V head-split; Z concatenated).
+struct AttnArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* Z;
+  int B, n_q, n_k, h, d_h, d_vh;
+  float c;
+  int causal;           // keys j <= i only
+  int padding;          // keys j < valid_len[b]
+  int pad_queries;      // rows i >= valid_len[b] are not computed (Z row = 0)
+  const int32_t* valid_len_host;  // B entries when padding
+  int32_t* err;
+};
+
+// Kernel limit for bounded waits (nanoseconds).
+uint64_t wait_limit_ns();
+void count_launch(int n = 1);
+
+// CUDA-core kernels (fp32; the bf16 instantiation is kept for tests).
+mha_status gemm_simt(const GemmProblem* probs, int nprob, mha_dtype dt, cudaStream_t s);
+mha_status attention_simt(const AttnArgs& a, mha_dtype dt, cudaStream_t s);
+
+// Tensor-core kernels (bf16).
+mha_status gemm_tc(const GemmProblem* probs, int nprob, int32_t* err, cudaStream_t s);
+mha_status attention_tc(const AttnArgs& a, cudaStream_t s);
+
+// TMA descriptors (cuTensorMapEncodeTiled through the runtime's driver entry
+// point). dims/strides innermost first; strides in bytes for dims 1..rank-1.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
+
+mha_status selftest_wait(int32_t* err, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace mha

@@ -1,0 +1,363 @@
+// mha_api.cu - the C ABI (include/mha.h): argument checks, workspace layout,
+// dispatch of the three steps, device error word, TMA descriptor encoding.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace mha {
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+// Bounded waits give up after this long. Long enough for any legitimate wait
+// (a whole kernel takes milliseconds), short enough to free a shared GPU fast.
+uint64_t wait_limit_ns() { return 2000000000ull; }
+
+// ---------------------------------------------------------------------------
+// TMA descriptors
+// ---------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                  d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Failure-detection self-test kernel
+// ---------------------------------------------------------------------------
+
+__global__ void selftest_wait_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);  // one arrival expected; nothing ever arrives
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtl w{err, &abort_flag, limit_ns};
+    mbar_wait(&bar, 0, w);
+  }
+  __syncthreads();
+}
+
+mha_status selftest_wait(int32_t* err, uint64_t limit_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+}  // namespace mha
+
+using namespace mha;
+
+namespace {
+
+constexpr size_t kHeader = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t elem_size(mha_dtype dt) { return dt == MHA_DTYPE_F32 ? 4 : 2; }
+
+bool dtype_ok(mha_dtype dt) { return dt == MHA_DTYPE_F32 || dt == MHA_DTYPE_BF16; }
+
+bool mask_ok(mha_mask_kind m) {
+  return m == MHA_MASK_NONE || m == MHA_MASK_CAUSAL || m == MHA_MASK_PADDING ||
+         m == MHA_MASK_CAUSAL_PADDING;
+}
+
+bool has_causal(mha_mask_kind m) { return m == MHA_MASK_CAUSAL || m == MHA_MASK_CAUSAL_PADDING; }
+bool has_padding(mha_mask_kind m) {
+  return m == MHA_MASK_PADDING || m == MHA_MASK_CAUSAL_PADDING;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  size_t q, k, v, z, total;
+};
+
+Layout layout(int B, int n_q, int n_k, int h, int d_h, int d_vh, mha_dtype dt) {
+  const size_t es = elem_size(dt);
+  Layout L;
+  L.q = kHeader;
+  L.k = align_up(L.q + (size_t)B * h * n_q * d_h * es, 1024);
+  L.v = align_up(L.k + (size_t)B * h * n_k * d_h * es, 1024);
+  L.z = align_up(L.v + (size_t)B * h * n_k * d_vh * es, 1024);
+  L.total = align_up(L.z + (size_t)B * n_q * h * d_vh * es, 1024);
+  return L;
+}
+
+// Shape support of each compute path (MHA_OK or MHA_ERR_UNSUPPORTED).
+mha_status check_head_dims(int d_h, int d_vh, mha_dtype dt) {
+  if (dt == MHA_DTYPE_BF16) {
+    if ((d_h != 64 && d_h != 128) || (d_vh != 64 && d_vh != 128)) return MHA_ERR_UNSUPPORTED;
+  } else {
+    if (d_h > 128 || d_vh > 128) return MHA_ERR_UNSUPPORTED;
+  }
+  return MHA_OK;
+}
+
+// Elements beyond 2^31 per tensor are not addressed by every index path.
+bool fits(long long a, long long b, long long c) {
+  const long long lim = (1ll << 31) - 1;
+  return a > 0 && b > 0 && c > 0 && a <= lim / b && a * b <= lim / c;
+}
+
+mha_status check_valid_len(mha_mask_kind mask, const int32_t* valid_len, int B, int n_k) {
+  if (!has_padding(mask)) return MHA_OK;
+  if (!valid_len) return MHA_ERR_INVALID_ARG;
+  if (B > MHA_MAX_PADDED_BATCH) return MHA_ERR_UNSUPPORTED;
+  for (int b = 0; b < B; ++b)
+    if (valid_len[b] < 1 || valid_len[b] > n_k) return MHA_ERR_EMPTY_ROW;
+  return MHA_OK;
+}
+
+mha_status run_qkv(const void* X_q, const void* X_kv, const void* W_Q, const void* W_K,
+                   const void* W_V, void* Q, void* K, void* V, int B, int n_q, int n_k,
+                   int d_model, int h, int d_h, int d_vh, mha_dtype dt, int32_t* err,
+                   cudaStream_t s) {
+  const void* Xk = X_kv ? X_kv : X_q;
+  GemmProblem p[3] = {
+      head_split_problem(X_q, W_Q, Q, B, n_q, h, d_h, d_model),
+      head_split_problem(Xk, W_K, K, B, n_k, h, d_h, d_model),
+      head_split_problem(Xk, W_V, V, B, n_k, h, d_vh, d_model),
+  };
+  if (dt == MHA_DTYPE_BF16) return gemm_tc(p, 3, err, s);
+  return gemm_simt(p, 3, dt, s);
+}
+
+mha_status run_attention(const AttnArgs& a, mha_dtype dt, cudaStream_t s) {
+  if (dt == MHA_DTYPE_BF16) return attention_tc(a, s);
+  return attention_simt(a, dt, s);
+}
+
+mha_status run_out(const void* Z, const void* W_O, void* Y, int B, int n_q, int h, int d_vh,
+                   int d_o, mha_dtype dt, int32_t* err, cudaStream_t s) {
+  GemmProblem p = plain_problem(Z, W_O, Y, B * n_q, d_o, h * d_vh);
+  if (dt == MHA_DTYPE_BF16) return gemm_tc(&p, 1, err, s);
+  return gemm_simt(&p, 1, dt, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int d_h, int d_vh,
+                          int d_o, mha_dtype dt) {
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0 ||
+      d_o <= 0 || !dtype_ok(dt))
+    return 0;
+  return layout(B, n_q, n_k, h, d_h, d_vh, dt).total;
+}
+
+mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h, int d_vh,
+                                mha_dtype dt, size_t offsets[6]) {
+  if (!offsets || B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0 ||
+      !dtype_ok(dt))
+    return MHA_ERR_INVALID_ARG;
+  const Layout L = layout(B, n_q, n_k, h, d_h, d_vh, dt);
+  offsets[0] = 0;
+  offsets[1] = L.q;
+  offsets[2] = L.k;
+  offsets[3] = L.v;
+  offsets[4] = L.z;
+  offsets[5] = L.total;
+  return MHA_OK;
+}
+
+mha_status mha_qkv_projection(const void* X_q, const void* X_kv, const void* W_Q,
+                              const void* W_K, const void* W_V, void* Q, void* K, void* V,
+                              int B, int n_q, int n_k, int d_model, int h, int d_h, int d_vh,
+                              mha_dtype dt, int32_t* dev_error, void* stream) {
+  if (!X_q || !W_Q || !W_K || !W_V || !Q || !K || !V) return MHA_ERR_INVALID_ARG;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
+    return MHA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt)) return MHA_ERR_INVALID_ARG;
+  if (!X_kv && n_k != n_q) return MHA_ERR_INVALID_ARG;
+  mha_status st = check_head_dims(d_h, d_vh, dt);
+  if (st != MHA_OK) return st;
+  if (!fits(B, n_q, d_model) || !fits(B, n_k, d_model) || !fits(B, n_q, h * d_h) ||
+      !fits(B, n_k, h * (long long)d_vh))
+    return MHA_ERR_UNSUPPORTED;
+  if (dt == MHA_DTYPE_BF16) {
+    if (d_model % 8 || !aligned16(X_q) || (X_kv && !aligned16(X_kv)) || !aligned16(W_Q) ||
+        !aligned16(W_K) || !aligned16(W_V) || !aligned16(Q) || !aligned16(K) || !aligned16(V))
+      return MHA_ERR_UNSUPPORTED;
+  }
+  return run_qkv(X_q, X_kv, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_model, h, d_h, d_vh, dt,
+                 dev_error, static_cast<cudaStream_t>(stream));
+}
+
+mha_status mha_attention(const void* Q, const void* K, const void* V, void* Z, int B, int n_q,
+                         int n_k, int h, int d_h, int d_vh, float c, mha_mask_kind mask,
+                         const int32_t* valid_len, int self_attention, mha_dtype dt,
+                         int32_t* dev_error, void* stream) {
+  if (!Q || !K || !V || !Z) return MHA_ERR_INVALID_ARG;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
+    return MHA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt) || !mask_ok(mask) || !isfinite(c)) return MHA_ERR_INVALID_ARG;
+  if (has_causal(mask) && n_q != n_k) return MHA_ERR_INVALID_ARG;
+  if (self_attention && n_q != n_k) return MHA_ERR_INVALID_ARG;
+  mha_status st = check_valid_len(mask, valid_len, B, n_k);
+  if (st != MHA_OK) return st;
+  st = check_head_dims(d_h, d_vh, dt);
+  if (st != MHA_OK) return st;
+  if (!fits((long long)B * h, n_q, d_h) || !fits((long long)B * h, n_k, d_h) ||
+      !fits((long long)B * h, n_k, d_vh) || !fits((long long)B * h, n_q, d_vh))
+    return MHA_ERR_UNSUPPORTED;
+  if (dt == MHA_DTYPE_BF16 &&
+      (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Z)))
+    return MHA_ERR_UNSUPPORTED;
+  AttnArgs a{};
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.Z = Z;
+  a.B = B;
+  a.n_q = n_q;
+  a.n_k = n_k;
+  a.h = h;
+  a.d_h = d_h;
+  a.d_vh = d_vh;
+  a.c = c;
+  a.causal = has_causal(mask);
+  a.padding = has_padding(mask);
+  a.pad_queries = has_padding(mask) && self_attention;
+  a.valid_len_host = valid_len;
+  a.err = dev_error;
+  return run_attention(a, dt, static_cast<cudaStream_t>(stream));
+}
+
+mha_status mha_output_projection(const void* Z, const void* W_O, void* Y, int B, int n_q, int h,
+                                 int d_vh, int d_o, mha_dtype dt, int32_t* dev_error,
+                                 void* stream) {
+  if (!Z || !W_O || !Y) return MHA_ERR_INVALID_ARG;
+  if (B <= 0 || n_q <= 0 || h <= 0 || d_vh <= 0 || d_o <= 0) return MHA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt)) return MHA_ERR_INVALID_ARG;
+  if (!fits(B, n_q, (long long)h * d_vh) || !fits(B, n_q, d_o)) return MHA_ERR_UNSUPPORTED;
+  if (dt == MHA_DTYPE_BF16 &&
+      ((h * d_vh) % 8 || d_o % 8 || !aligned16(Z) || !aligned16(W_O) || !aligned16(Y)))
+    return MHA_ERR_UNSUPPORTED;
+  return run_out(Z, W_O, Y, B, n_q, h, d_vh, d_o, dt, dev_error,
+                 static_cast<cudaStream_t>(stream));
+}
+
+mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q, const void* W_K,
+                       const void* W_V, const void* W_O, void* Y, int B, int n_q, int n_k,
+                       int d_model, int h, int d_h, int d_vh, int d_o, float c,
+                       mha_mask_kind mask, const int32_t* valid_len, mha_dtype dt,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  // Host-side checks, all before anything is enqueued.
+  if (!X_q || !W_Q || !W_K || !W_V || !W_O || !Y) return MHA_ERR_INVALID_ARG;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0 ||
+      d_o <= 0)
+    return MHA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt) || !mask_ok(mask) || !isfinite(c)) return MHA_ERR_INVALID_ARG;
+  const bool self_attn = X_kv == nullptr;
+  if (self_attn && n_k != n_q) return MHA_ERR_INVALID_ARG;
+  if (has_causal(mask) && n_q != n_k) return MHA_ERR_INVALID_ARG;
+  mha_status st = check_valid_len(mask, valid_len, B, n_k);
+  if (st != MHA_OK) return st;
+  st = check_head_dims(d_h, d_vh, dt);
+  if (st != MHA_OK) return st;
+  if (dt == MHA_DTYPE_BF16 && (d_model % 8 || d_o % 8)) return MHA_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MHA_ERR_WORKSPACE;
+  const Layout L = layout(B, n_q, n_k, h, d_h, d_vh, dt);
+  if (workspace_bytes < L.total) return MHA_ERR_WORKSPACE;
+  if (dt == MHA_DTYPE_BF16 && (!aligned16(X_q) || (X_kv && !aligned16(X_kv)) ||
+                               !aligned16(W_Q) || !aligned16(W_K) || !aligned16(W_V) ||
+                               !aligned16(W_O) || !aligned16(Y)))
+    return MHA_ERR_UNSUPPORTED;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int32_t* err = reinterpret_cast<int32_t*>(ws);
+  void* Q = ws + L.q;
+  void* K = ws + L.k;
+  void* V = ws + L.v;
+  void* Z = ws + L.z;
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return MHA_ERR_CUDA;
+  st = mha_qkv_projection(X_q, X_kv, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_model, h, d_h,
+                          d_vh, dt, err, stream);
+  if (st != MHA_OK) return st;
+  st = mha_attention(Q, K, V, Z, B, n_q, n_k, h, d_h, d_vh, c, mask, valid_len,
+                     self_attn ? 1 : 0, dt, err, stream);
+  if (st != MHA_OK) return st;
+  return mha_output_projection(Z, W_O, Y, B, n_q, h, d_vh, d_o, dt, err, stream);
+}
+
+mha_status mha_get_device_error(void* error_word, void* stream) {
+  if (!error_word) return MHA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, error_word, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MHA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MHA_ERR_CUDA;
+  if (v != 0 && cudaMemsetAsync(error_word, 0, sizeof(int32_t), s) != cudaSuccess)
+    return MHA_ERR_CUDA;
+  return static_cast<mha_status>(v);
+}
+
+const char* mha_status_string(mha_status s) {
+  switch (s) {
+    case MHA_OK: return "ok";
+    case MHA_ERR_INVALID_ARG: return "invalid argument";
+    case MHA_ERR_UNSUPPORTED: return "unsupported shape, alignment or size";
+    case MHA_ERR_EMPTY_ROW: return "a query row has no allowed key (valid length outside [1, n_k])";
+    case MHA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MHA_ERR_CUDA: return "CUDA runtime or launch error";
+    case MHA_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on one of its barriers";
+  }
+  return "unknown status";
+}
+
+mha_status mha_selftest_wait_timeout(int32_t* dev_error, uint64_t limit_ns, void* stream) {
+  if (!dev_error) return MHA_ERR_INVALID_ARG;
+  if (limit_ns < 1000ull) limit_ns = 1000ull;
+  if (limit_ns > 10000000000ull) limit_ns = 10000000000ull;
+  return selftest_wait(dev_error, limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+uint64_t mha_kernel_launch_count(void) { return g_launches.load(); }
+
+const char* mha_version(void) { return "head_scaled_dot_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+"""Python binding of the C ABI in include/mha.h (ctypes).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+library. torch supplies device memory, the current stream and tensor
+metadata. If the library has not been built, loading raises: there is no
+fallback path.
+"""
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmha_gb300.so")
+
+MHA_OK = 0
+STATUS_NAMES = {
+    0: "MHA_OK",
+    1: "MHA_ERR_INVALID_ARG",
+    2: "MHA_ERR_UNSUPPORTED",
+    3: "MHA_ERR_EMPTY_ROW",
+    4: "MHA_ERR_WORKSPACE",
+    5: "MHA_ERR_CUDA",
+    6: "MHA_ERR_DEVICE_TIMEOUT",
+}
+MASKS = {"none": 0, "causal": 1, "padding": 2, "causal_padding": 3}
+DTYPES = {"f32": 0, "bf16": 1}
+TORCH_DTYPES = {torch.float32: "f32", torch.bfloat16: "bf16"}
+
+# Symbols declared in include/mha.h.
+EXPORTS = (
+    "mha_workspace_size", "mha_workspace_layout", "mha_forward", "mha_qkv_projection", "mha_attention",
+    "mha_output_projection", "mha_get_device_error", "mha_status_string",
+    "mha_selftest_wait_timeout", "mha_kernel_launch_count", "mha_version",
+)
+
+_lib = None
+
+
+class MHAError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (what, STATUS_NAMES.get(status, status),
+                                         status_string(status) if _lib else ""))
+
+
+def load(path=LIB_PATH):
+    """Loads the shared library once and declares the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError("libmha_gb300.so is not built (run __graft_entry__.build()): " + path)
+    lib = ctypes.CDLL(path)
+    P, I, F, S, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+    lib.mha_workspace_size.restype = S
+    lib.mha_workspace_size.argtypes = [I] * 8 + [I]
+    lib.mha_workspace_layout.restype = I
+    lib.mha_workspace_layout.argtypes = [I] * 6 + [I, ctypes.POINTER(S)]
+    lib.mha_forward.restype = I
+    lib.mha_forward.argtypes = [P] * 7 + [I] * 8 + [F, I, P, I, P, S, P]
+    lib.mha_qkv_projection.restype = I
+    lib.mha_qkv_projection.argtypes = [P] * 8 + [I] * 7 + [I, P, P]
+    lib.mha_attention.restype = I
+    lib.mha_attention.argtypes = [P] * 4 + [I] * 6 + [F, I, P, I, I, P, P]
+    lib.mha_output_projection.restype = I
+    lib.mha_output_projection.argtypes = [P] * 3 + [I] * 5 + [I, P, P]
+    lib.mha_get_device_error.restype = I
+    lib.mha_get_device_error.argtypes = [P, P]
+    lib.mha_status_string.restype = ctypes.c_char_p
+    lib.mha_status_string.argtypes = [I]
+    lib.mha_selftest_wait_timeout.restype = I
+    lib.mha_selftest_wait_timeout.argtypes = [P, U64, P]
+    lib.mha_kernel_launch_count.restype = U64
+    lib.mha_kernel_launch_count.argtypes = []
+    lib.mha_version.restype = ctypes.c_char_p
+    lib.mha_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load().mha_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, what):
+    if status != MHA_OK:
+        raise MHAError(status, what)
+
+
+def _lens(valid_len, B):
+    """Host int32 array of valid lengths (or None) and the object keeping it alive."""
+    if valid_len is None:
+        return None, None
+    arr = (ctypes.c_int32 * B)(*[int(x) for x in list(valid_len)[:B]])
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def workspace_size(B, n_q, n_k, d_model, h, d_h, d_vh, d_o, dtype):
+    return int(load().mha_workspace_size(B, n_q, n_k, d_model, h, d_h, d_vh, d_o, DTYPES[dtype]))
+
+
+def workspace_layout(B, n_q, n_k, h, d_h, d_vh, dtype):
+    """Byte offsets of the error word, Q, K, V, Z and the total size."""
+    off = (ctypes.c_size_t * 6)()
+    _check(load().mha_workspace_layout(B, n_q, n_k, h, d_h, d_vh, DTYPES[dtype], off),
+           "mha_workspace_layout")
+    return dict(zip(("err", "q", "k", "v", "z", "total"), [int(x) for x in off]))
+
+
+def launch_count():
+    return int(load().mha_kernel_launch_count())
+
+
+def forward(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, mask="none", valid_len=None,
+            out=None, workspace=None, stream=None, check=True):
+    """Y = MHA(X_q, X_kv) on the GPU. Tensors: CUDA, contiguous, one dtype
+    (float32 or bfloat16). X_kv None means self-attention. Returns Y
+    (B, n_q, d_o); with check=True the device error word is read back
+    (one stream synchronisation)."""
+    lib = load()
+    B, n_q, d_model = X_q.shape
+    n_k = n_q if X_kv is None else X_kv.shape[1]
+    d_o = W_O.shape[1]
+    dt = TORCH_DTYPES[X_q.dtype]
+    if out is None:
+        out = torch.empty((B, n_q, d_o), dtype=X_q.dtype, device=X_q.device)
+    ws_bytes = workspace_size(B, n_q, n_k, d_model, h, d_h, d_vh, d_o, dt)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=X_q.device)
+    lens, keep = _lens(valid_len, B)
+    st = lib.mha_forward(_ptr(X_q), _ptr(X_kv), _ptr(W_Q), _ptr(W_K), _ptr(W_V), _ptr(W_O),
+                         _ptr(out), B, n_q, n_k, d_model, h, d_h, d_vh, d_o, float(c),
+                         MASKS[mask], lens, DTYPES[dt], _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    del keep
+    _check(st, "mha_forward")
+    if check:
+        _check(lib.mha_get_device_error(_ptr(workspace), _stream(stream)), "mha_forward (device)")
+    return out
+
+
+def qkv_projection(X_q, X_kv, W_Q, W_K, W_V, h, d_h, d_vh, dev_error=None, stream=None):
+    """Step 1: head-split Q (B,h,n_q,d_h), K (B,h,n_k,d_h), V (B,h,n_k,d_vh)."""
+    lib = load()
+    B, n_q, d_model = X_q.shape
+    n_k = n_q if X_kv is None else X_kv.shape[1]
+    dt = TORCH_DTYPES[X_q.dtype]
+    kw = dict(dtype=X_q.dtype, device=X_q.device)
+    Q = torch.empty((B, h, n_q, d_h), **kw)
+    K = torch.empty((B, h, n_k, d_h), **kw)
+    V = torch.empty((B, h, n_k, d_vh), **kw)
+    st = lib.mha_qkv_projection(_ptr(X_q), _ptr(X_kv), _ptr(W_Q), _ptr(W_K), _ptr(W_V),
+                                _ptr(Q), _ptr(K), _ptr(V), B, n_q, n_k, d_model, h, d_h, d_vh,
+                                DTYPES[dt], _ptr(dev_error), _stream(stream))
+    _check(st, "mha_qkv_projection")
+    return Q, K, V
+
+
+def attention(Q, K, V, c, mask="none", valid_len=None, self_attention=True, out=None,
+              dev_error=None, stream=None):
+    """Step 2: Z (B, n_q, h*d_vh) from head-split Q, K, V."""
+    lib = load()
+    B, h, n_q, d_h = Q.shape
+    n_k, d_vh = V.shape[2], V.shape[3]
+    dt = TORCH_DTYPES[Q.dtype]
+    if out is None:
+        out = torch.empty((B, n_q, h * d_vh), dtype=Q.dtype, device=Q.device)
+    lens, keep = _lens(valid_len, B)
+    st = lib.mha_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, n_q, n_k, h, d_h, d_vh,
+                           float(c), MASKS[mask], lens, int(bool(self_attention)), DTYPES[dt],
+                           _ptr(dev_error), _stream(stream))
+    del keep
+    _check(st, "mha_attention")
+    return out
+
+
+def output_projection(Z, W_O, h, d_vh, out=None, dev_error=None, stream=None):
+    """Step 3: Y = Z W_O."""
+    lib = load()
+    B, n_q, _ = Z.shape
+    d_o = W_O.shape[1]
+    dt = TORCH_DTYPES[Z.dtype]
+    if out is None:
+        out = torch.empty((B, n_q, d_o), dtype=Z.dtype, device=Z.device)
+    st = lib.mha_output_projection(_ptr(Z), _ptr(W_O), _ptr(out), B, n_q, h, d_vh, d_o,
+                                   DTYPES[dt], _ptr(dev_error), _stream(stream))
+    _check(st, "mha_output_projection")
+    return out
+
+
+def get_device_error(error_word, stream=None):
+    """Reads and resets a device error word; returns the status code."""
+    return int(load().mha_get_device_error(_ptr(error_word), _stream(stream)))
+
+
+def selftest_wait_timeout(dev_error, limit_ns, stream=None):
+    _check(load().mha_selftest_wait_timeout(_ptr(dev_error), int(limit_ns), _stream(stream)),
+           "mha_selftest_wait_timeout")

@@ -1,0 +1,215 @@
+/*
+ * mha.h - C ABI of the GB300 multi-head attention forward pass.
+ *
+ * The layer (the "Multi-head attention and self-attention" Definition on
+ * alphabetamath.cc, and the "The Complete Multi-Head Operation" section of
+ * the llmprimer.com multi-head attention review):
+ *
+ *   head i:  H_i = softmax( c * (X_q W_i^Q)(X_kv W_i^K)^T + M ) (X_kv W_i^V)
+ *   output:  Y   = Concat_feature(H_1, ..., H_h) W^O
+ *
+ * computed on one GPU in three steps, each also exported on its own:
+ *   1. mha_qkv_projection   - combined projections with the head split
+ *                             (B,T,h*d) -> (B,h,T,d) done in the GEMM epilogue;
+ *   2. mha_attention        - the fused attention kernel: key blocks are folded
+ *                             into the stable summary (m, l, z) with its merge
+ *                             ("Stable summary of an attention key block",
+ *                             Definition), z / l is taken once per row, and the
+ *                             B x h x n_q x n_k score tensor is never stored;
+ *   3. mha_output_projection - Y = Z W^O.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensors are dense, row-major, batch-major ("The Complete Multi-Head
+ *   Operation": X : B x T x d_model, Z : B x T x (h d_v), Y : B x T x d_model).
+ * - Weights are used as given, right-multiplied (X W), in the combined form of
+ *   "Separate and Combined Projections": W_Q, W_K are d_model x (h*d_h) and
+ *   W_V is d_model x (h*d_vh); head i owns columns [i*d, (i+1)*d). W_O is
+ *   (h*d_vh) x d_o; head i owns rows [i*d_vh, (i+1)*d_vh). No biases.
+ * - Element type: MHA_DTYPE_BF16 (inputs, intermediates and Y in bf16,
+ *   accumulation in fp32, tensor cores) or MHA_DTYPE_F32 (everything fp32,
+ *   CUDA-core FMA kernels).
+ * - Pointers named X_*, W_*, Q, K, V, Z, Y and the workspace are DEVICE
+ *   pointers owned by the caller; the library keeps none of them after the
+ *   call returns and allocates no device memory. `valid_len` is a HOST array.
+ *   Every device pointer must be 16-byte aligned. Outputs must not alias
+ *   inputs; X_kv may equal X_q.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream). Every call is
+ *   asynchronous on that stream: it validates its arguments on the host,
+ *   enqueues its kernels and returns.
+ * - Masks ("From Attention to Self-Attention review", "Causal and padding
+ *   masks"; masked positions get weight exactly 0):
+ *     MHA_MASK_NONE            every query row uses every key;
+ *     MHA_MASK_CAUSAL          row i uses keys j <= i (needs n_q == n_k);
+ *     MHA_MASK_PADDING         batch item b uses keys j < valid_len[b];
+ *     MHA_MASK_CAUSAL_PADDING  both.
+ *   In self-attention (X_kv == NULL) with a padding mask the query rows
+ *   i >= valid_len[b] are padding as well: they are not computed and their
+ *   rows of Z and Y are written as exact zeros. In cross-attention the
+ *   padding applies to keys only.
+ * - Every query row must keep at least one allowed key (the nonempty allowed
+ *   set of the block-summary Definition): valid_len[b] must lie in
+ *   [1, n_k], else the call returns MHA_ERR_EMPTY_ROW and launches nothing.
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; on
+ * any error nothing is launched and the outputs are untouched. A kernel that
+ * waits too long on one of its own barriers gives up, records
+ * MHA_ERR_DEVICE_TIMEOUT in the caller's device error word and returns; read it
+ * with mha_get_device_error.
+ */
+#ifndef MHA_GB300_H
+#define MHA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MHA_API __attribute__((visibility("default")))
+#else
+#define MHA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MHA_OK = 0,
+  MHA_ERR_INVALID_ARG = 1,    /* a NULL or non-positive argument, a bad enum, non-finite c */
+  MHA_ERR_UNSUPPORTED = 2,    /* a valid shape this build does not handle (see mha_forward) */
+  MHA_ERR_EMPTY_ROW = 3,      /* some query row would have no allowed key */
+  MHA_ERR_WORKSPACE = 4,      /* workspace NULL, misaligned or smaller than mha_workspace_size */
+  MHA_ERR_CUDA = 5,           /* a CUDA runtime call or a launch failed */
+  MHA_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up waiting on one of its barriers */
+} mha_status;
+
+typedef enum {
+  MHA_MASK_NONE = 0,
+  MHA_MASK_CAUSAL = 1,
+  MHA_MASK_PADDING = 2,
+  MHA_MASK_CAUSAL_PADDING = 3
+} mha_mask_kind;
+
+typedef enum { MHA_DTYPE_F32 = 0, MHA_DTYPE_BF16 = 1 } mha_dtype;
+
+/* Largest batch accepted together with a padding mask (the valid lengths
+ * travel to the kernels inside their launch parameters). */
+#define MHA_MAX_PADDED_BATCH 1024
+
+/*
+ * Bytes of device workspace mha_forward needs for these sizes: the head-split
+ * Q, K (B*h*n*d_h elements), V (B*h*n_k*d_vh), the concatenated Z
+ * (B*n_q*h*d_vh) and a 256-byte header whose first int32 is the device error
+ * word. Linear in n_q and n_k: no term grows with n_q * n_k. Returns 0 when an
+ * argument is non-positive or the dtype is unknown.
+ */
+MHA_API size_t mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int d_h,
+                          int d_vh, int d_o, mha_dtype dt);
+
+/*
+ * Byte offsets inside the workspace of mha_forward, for callers that want to
+ * inspect the intermediates or run the three steps themselves on the same
+ * buffers: offsets[0] the int32 device error word, [1] Q, [2] K, [3] V, [4] Z,
+ * [5] the total size (= mha_workspace_size). Returns MHA_ERR_INVALID_ARG on a
+ * non-positive size, an unknown dtype or a NULL `offsets`.
+ */
+MHA_API mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h, int d_vh,
+                                        mha_dtype dt, size_t offsets[6]);
+
+/*
+ * The whole forward pass: Y = MHA(X_q, X_kv).
+ *
+ *   X_q   (B, n_q, d_model)      queries' token matrix
+ *   X_kv  (B, n_k, d_model)      keys' and values' token matrix; NULL means
+ *                                self-attention (X_kv := X_q, needs n_k == n_q)
+ *   W_Q, W_K (d_model, h*d_h), W_V (d_model, h*d_vh), W_O (h*d_vh, d_o)
+ *   Y     (B, n_q, d_o)          output
+ *   c                            score scale (finite; 1/sqrt(d_h) is usual)
+ *   valid_len                    HOST int32[B] for the padding masks, else
+ *                                ignored (may be NULL)
+ *   workspace, workspace_bytes   device scratch of at least
+ *                                mha_workspace_size(...) bytes, 256-byte
+ *                                aligned; its contents on entry do not matter
+ *
+ * bf16 limits (MHA_ERR_UNSUPPORTED otherwise): d_h and d_vh in {64, 128};
+ * d_model and d_o multiples of 8. f32 limits: d_h, d_vh <= 128.
+ * Enqueues a 4-byte memset of the error word and three kernels.
+ */
+MHA_API mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q,
+                       const void* W_K, const void* W_V, const void* W_O,
+                       void* Y, int B, int n_q, int n_k, int d_model, int h,
+                       int d_h, int d_vh, int d_o, float c, mha_mask_kind mask,
+                       const int32_t* valid_len, mha_dtype dt, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Step 1: combined projections with the head split ("Separate and Combined
+ * Projections": (B,T,h d) -> (B,T,h,d) -> (B,h,T,d)).
+ *   Q (B, h, n_q, d_h) = head split of X_q W_Q
+ *   K (B, h, n_k, d_h) = head split of X_kv W_K
+ *   V (B, h, n_k, d_vh) = head split of X_kv W_V
+ * X_kv NULL means X_kv := X_q (n_k must equal n_q). dev_error: device int32
+ * error word (may be NULL: timeouts then go unreported).
+ */
+MHA_API mha_status mha_qkv_projection(const void* X_q, const void* X_kv,
+                              const void* W_Q, const void* W_K, const void* W_V,
+                              void* Q, void* K, void* V, int B, int n_q,
+                              int n_k, int d_model, int h, int d_h, int d_vh,
+                              mha_dtype dt, int32_t* dev_error, void* stream);
+
+/*
+ * Step 2: fused masked attention on head-split inputs, written in the
+ * concatenated layout ("reverse the head-position transpose", then
+ * "Concatenate along the head-feature axis in the declared order").
+ *   Q (B, h, n_q, d_h), K (B, h, n_k, d_h), V (B, h, n_k, d_vh)
+ *   Z (B, n_q, h*d_vh): Z[b, i, j*d_vh + r] = head j's output row i, column r
+ * self_attention != 0 marks the padded query rows (i >= valid_len[b]) as not
+ * computed (their Z rows are 0); 0 applies padding to keys only.
+ */
+MHA_API mha_status mha_attention(const void* Q, const void* K, const void* V, void* Z,
+                         int B, int n_q, int n_k, int h, int d_h, int d_vh,
+                         float c, mha_mask_kind mask, const int32_t* valid_len,
+                         int self_attention, mha_dtype dt, int32_t* dev_error,
+                         void* stream);
+
+/*
+ * Step 3: Y (B*n_q, d_o) = Z (B*n_q, h*d_vh) W_O (h*d_vh, d_o)
+ * ("The Complete Multi-Head Operation": Y = Z W_O).
+ */
+MHA_API mha_status mha_output_projection(const void* Z, const void* W_O, void* Y,
+                                 int B, int n_q, int h, int d_vh, int d_o,
+                                 mha_dtype dt, int32_t* dev_error,
+                                 void* stream);
+
+/*
+ * Reads the device error word (the workspace base for mha_forward, or the
+ * dev_error given to a step), waits for `stream`, resets the word to 0 and
+ * returns what it held (MHA_OK when no kernel reported a problem), or
+ * MHA_ERR_CUDA if the copy itself failed.
+ */
+MHA_API mha_status mha_get_device_error(void* error_word, void* stream);
+
+/* A fixed English description of a status code. Never NULL. */
+MHA_API const char* mha_status_string(mha_status s);
+
+/*
+ * Failure-detection self-test: launches one CTA whose thread waits on a
+ * barrier that nothing completes, through the same bounded wait the kernels
+ * use, with a limit of `limit_ns` nanoseconds (clamped to [1e3, 1e10]). The
+ * kernel must give up, write MHA_ERR_DEVICE_TIMEOUT to *dev_error and return,
+ * leaving the context usable.
+ */
+MHA_API mha_status mha_selftest_wait_timeout(int32_t* dev_error, uint64_t limit_ns,
+                                     void* stream);
+
+/* Number of kernels this library has enqueued since it was loaded. */
+MHA_API uint64_t mha_kernel_launch_count(void);
+
+/* Library version string. */
+MHA_API const char* mha_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_GB300_H */

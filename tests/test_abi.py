@@ -1,0 +1,123 @@
+"""The C ABI on the CPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before touching CUDA."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mha.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from head_scaled_dot_gb300 import mha
+    if not os.path.exists(mha.LIB_PATH):
+        from head_scaled_dot_gb300 import build
+        build.build()
+    return mha.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"MHA_API\s+[\w\s\*]+?\b(mha_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["mha_forward", "mha_workspace_size", "mha_status_string", "mha_get_device_error",
+              "mha_qkv_projection", "mha_attention", "mha_output_projection"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from head_scaled_dot_gb300 import mha
+    names = declared_functions()
+    assert set(names) == set(mha.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from head_scaled_dot_gb300 import mha
+    for code in range(7):
+        s = mha.status_string(code)
+        assert s and s != "unknown status"
+    assert mha.status_string(99) == "unknown status"
+
+
+def test_workspace_size_is_linear_in_sequence_lengths(lib):
+    from head_scaled_dot_gb300 import mha
+    ws = lambda nq, nk: mha.workspace_size(2, nq, nk, 256, 4, 64, 64, 256, "bf16")
+    base = ws(1024, 1024)
+    # doubling both lengths at most doubles the bytes (plus alignment): no n_q*n_k term
+    assert ws(2048, 2048) <= 2 * base + 4096
+    assert ws(8192, 8192) <= 8 * base + 4 * 8192
+    exact = 256 + 2 * 4 * (1024 * 64 * 3 + 1024 * 64) * 2
+    assert exact <= base <= exact + 4 * 1024
+    assert mha.workspace_size(0, 1, 1, 1, 1, 1, 1, 1, "bf16") == 0
+
+
+def _fwd(lib, **kw):
+    """mha_forward with plausible non-null fake pointers: every call here must be
+    rejected by the host checks, which run before any CUDA call."""
+    from head_scaled_dot_gb300 import mha
+    a = dict(X_q=4096, X_kv=None, W_Q=8192, W_K=12288, W_V=16384, W_O=20480, Y=24576,
+             B=2, n_q=64, n_k=64, d_model=128, h=2, d_h=64, d_vh=64, d_o=128, c=0.125,
+             mask=0, valid_len=None, dt=1, ws=1 << 20, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.mha_forward(P(a["X_q"]), P(a["X_kv"]), P(a["W_Q"]), P(a["W_K"]), P(a["W_V"]),
+                           P(a["W_O"]), P(a["Y"]), a["B"], a["n_q"], a["n_k"], a["d_model"],
+                           a["h"], a["d_h"], a["d_vh"], a["d_o"], a["c"], a["mask"],
+                           a["valid_len"], a["dt"], P(a["ws"]), a["ws_bytes"], a["stream"])
+
+
+def _lens(*v):
+    arr = (ctypes.c_int32 * len(v))(*v)
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(X_q=None), 1), (dict(W_O=None), 1), (dict(Y=None), 1),
+    (dict(B=0), 1), (dict(n_q=-1), 1), (dict(h=0), 1), (dict(d_o=0), 1),
+    (dict(c=math.nan), 1), (dict(c=math.inf), 1), (dict(mask=7), 1), (dict(dt=5), 1),
+    (dict(n_k=65), 1),                       # self-attention needs n_k == n_q
+    (dict(X_kv=28672, n_k=65, mask=1), 1),   # causal needs n_q == n_k
+    (dict(mask=2), 1),                       # padding without valid lengths
+    (dict(d_h=96), 2), (dict(d_vh=32), 2), (dict(d_model=100), 2), (dict(d_o=12), 2),
+    (dict(d_h=192, dt=0), 2),
+    (dict(X_q=4097), 2),                     # bf16 pointers must be 16-byte aligned
+    (dict(ws=None), 4), (dict(ws=(1 << 20) + 16), 4), (dict(ws_bytes=1000), 4),
+])
+def test_forward_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def test_empty_allowed_rows_are_rejected(lib):
+    for v in [(0, 64), (64, 65), (-3, 10)]:
+        lens, keep = _lens(*v)
+        assert _fwd(lib, mask=2, valid_len=lens) == 3
+        assert _fwd(lib, mask=3, valid_len=lens) == 3
+    lens, keep = _lens(*([1] * 1025))
+    assert _fwd(lib, mask=2, valid_len=lens, B=1025) == 2
+
+
+def test_steps_reject_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    # attention: causal with n_q != n_k, non-finite c, padding without lengths
+    assert lib.mha_attention(P(16), P(32), P(48), P(64), 1, 8, 9, 1, 64, 64, 0.1, 1, None, 0,
+                             1, None, None) == 1
+    assert lib.mha_attention(P(16), P(32), P(48), P(64), 1, 8, 8, 1, 64, 64, math.nan, 0,
+                             None, 1, 1, None, None) == 1
+    assert lib.mha_attention(P(16), P(32), P(48), P(64), 1, 8, 8, 1, 64, 64, 0.1, 2, None, 1,
+                             1, None, None) == 1
+    assert lib.mha_output_projection(None, P(16), P(32), 1, 8, 1, 64, 64, 1, None, None) == 1
+    assert lib.mha_output_projection(P(16), P(32), P(48), 1, 8, 1, 64, 12, 1, None, None) == 2
+    assert lib.mha_qkv_projection(P(16), None, P(32), P(48), P(64), P(80), P(96), P(112), 1, 8,
+                                  9, 64, 1, 64, 64, 1, None, None) == 1
+    assert lib.mha_get_device_error(None, None) == 1
+    assert lib.mha_selftest_wait_timeout(None, 1000, None) == 1

@@ -1,0 +1,232 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs.
+
+Bar: max|Y - Y_ref| / max|Y_ref| over computed rows <= 1e-2 for bf16 and
+<= 1e-4 for fp32; padded query rows must be exactly zero.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from head_scaled_dot_gb300 import mha, workloads
+from helpers import TOL, computed_rows, f64, lens_list, oracle_forward, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return mha.load()
+
+
+def run(w, inp, **kw):
+    t = to_dev(inp)
+    Y = mha.forward(t["X_q"], t["X_kv"], t["W_Q"], t["W_K"], t["W_V"], t["W_O"], w.h, w.d_h,
+                    w.d_vh, w.c, w.mask, inp["valid_len"], **kw)
+    torch.cuda.synchronize()
+    return Y
+
+
+def check_full(w, inp, Y):
+    ref = oracle_forward(w, inp)
+    got = f64(Y)
+    assert np.isfinite(got).all()
+    rows = computed_rows(w, inp)
+    assert np.all(got[~rows] == 0.0), "padded query rows must be exactly zero"
+    err = rel_err(got[rows], ref[rows])
+    assert err <= TOL[w.dtype], "rel err %.3e > %.0e" % (err, TOL[w.dtype])
+    return err
+
+
+# ---------------------------------------------------------------------------
+# The five workloads at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("idx", [0, 1])
+def test_workload_full_compare(idx):
+    w = workloads.WORKLOADS[idx]
+    inp = workloads.make_inputs(w)
+    check_full(w, inp, run(w, inp))
+
+
+def sample_rows(w, L, rng, n=24):
+    hi = L if (L is not None and not w.cross) else w.n_q
+    cand = {0, 1, hi - 1, hi // 2, min(127, hi - 1), min(128, hi - 1)}
+    cand |= set(rng.integers(0, hi, n).tolist())
+    return sorted(c for c in cand if 0 <= c < hi)
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_workload_sampled_rows(idx):
+    w = workloads.WORKLOADS[idx]
+    inp = workloads.make_inputs(w)
+    got = f64(run(w, inp))
+    assert np.isfinite(got).all()
+    rows_ok = computed_rows(w, inp)
+    assert np.all(got[~rows_ok] == 0.0)
+    lens = lens_list(inp)
+    rng = np.random.default_rng(idx)
+    batches = range(w.B) if w.B <= 4 else sorted(set([0, w.B - 1] + rng.integers(0, w.B, 2).tolist()))
+    worst = 0.0
+    for b in batches:
+        L = None if lens is None else lens[b]
+        rows = sample_rows(w, L, rng)
+        Yr, _ = oracle.mha_rows(f64(inp["X_q"]), f64(inp["X_kv"]), f64(inp["W_Q"]),
+                                f64(inp["W_K"]), f64(inp["W_V"]), f64(inp["W_O"]), w.h, w.d_h,
+                                w.d_vh, w.c, oracle.MASK_NAMES[w.mask], lens, b, rows)
+        worst = max(worst, rel_err(got[b, rows], Yr))
+    assert worst <= TOL[w.dtype], "rel err %.3e" % worst
+
+
+# ---------------------------------------------------------------------------
+# Small and ragged shapes: several tiles plus a ragged tail, all masks
+# ---------------------------------------------------------------------------
+
+SHAPES = [
+    # B, n_q, n_k, d_model, h, d_h, d_vh, d_o, mask, cross, lengths
+    (2, 200, 200, 128, 2, 64, 64, 128, "causal", False, None),
+    (1, 1, 1, 64, 1, 64, 64, 64, "none", False, None),
+    (3, 130, 130, 256, 2, 128, 128, 192, "causal_padding", False, [1, 129, 130]),
+    (2, 77, 300, 64, 3, 64, 128, 136, "padding", True, [1, 300]),
+    (1, 256, 256, 512, 4, 128, 64, 512, "none", False, None),
+    (2, 100, 100, 64, 1, 64, 64, 64, "causal", False, None),
+    (2, 383, 383, 192, 2, 64, 64, 64, "padding", False, [383, 200]),
+    (1, 129, 517, 128, 2, 128, 128, 128, "none", True, None),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:8])) + "_" + s[8])
+def test_small_shapes(shape, dtype):
+    B, n_q, n_k, d_model, h, d_h, d_vh, d_o, mask, cross, lens = shape
+    w = workloads.Workload(name="small", B=B, n_q=n_q, n_k=n_k, d_model=d_model, h=h, d_h=d_h,
+                           d_vh=d_vh, d_o=d_o, mask=mask, dtype=dtype, cross=cross,
+                           c=1 / math.sqrt(d_h), seed=1000 + n_q)
+    inp = workloads.make_inputs(w, lengths=lens)
+    check_full(w, inp, run(w, inp))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("c", [0.0, -0.2, 0.9])
+def test_scale_special_cases(c, dtype):
+    w = workloads.Workload(name="scale", B=2, n_q=160, n_k=160, d_model=128, h=2, d_h=64,
+                           d_vh=64, d_o=128, mask="causal", dtype=dtype, cross=False, c=c, seed=7)
+    inp = workloads.make_inputs(w)
+    check_full(w, inp, run(w, inp))
+
+
+# ---------------------------------------------------------------------------
+# Step by step, in the audit order: Q/K/V, then Z, then Y
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_steps_against_oracle_intermediates(dtype):
+    w = workloads.Workload(name="steps", B=2, n_q=192, n_k=320, d_model=256, h=3, d_h=64,
+                           d_vh=128, d_o=64, mask="padding", dtype=dtype, cross=True,
+                           c=0.11, seed=5)
+    inp = workloads.make_inputs(w, lengths=[100, 320])
+    t = to_dev(inp)
+    ref_Y, inter = oracle_forward(w, inp, return_intermediates=True)
+    Q, K, V = mha.qkv_projection(t["X_q"], t["X_kv"], t["W_Q"], t["W_K"], t["W_V"], w.h, w.d_h,
+                                 w.d_vh)
+    for name, got in (("Q", Q), ("K", K), ("V", V)):
+        assert rel_err(f64(got), inter[name]) <= TOL[dtype], name
+    Z = mha.attention(Q, K, V, w.c, w.mask, lens_list(inp), self_attention=False)
+    assert rel_err(f64(Z), inter["Z"]) <= TOL[dtype]
+    Y = mha.output_projection(Z, t["W_O"], w.h, w.d_vh)
+    torch.cuda.synchronize()
+    assert rel_err(f64(Y), ref_Y) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("d", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("mask", ["none", "causal", "causal_padding"])
+def test_attention_step_alone(d, mask):
+    """The attention kernel on bf16 Q, K, V given directly; the oracle sees the
+    same bf16 values."""
+    d_h, d_vh = d
+    B, h, n = 2, 3, 333
+    g = torch.Generator().manual_seed(d_h + d_vh + len(mask))
+    Q = torch.randn((B, h, n, d_h), generator=g).bfloat16()
+    K = torch.randn((B, h, n, d_h), generator=g).bfloat16()
+    V = torch.randn((B, h, n, d_vh), generator=g).bfloat16()
+    lens = [333, 150] if "padding" in mask else None
+    c = 1 / math.sqrt(d_h)
+    Z = mha.attention(Q.cuda(), K.cuda(), V.cuda(), c, mask, lens, self_attention=True)
+    torch.cuda.synchronize()
+    got = f64(Z)
+    ref = np.zeros((B, n, h * d_vh))
+    for b in range(B):
+        L = None if lens is None else lens[b]
+        rows = oracle.query_rows_computed(oracle.MASK_NAMES[mask], n, L, True)
+        allowed = oracle.allowed_keys(oracle.MASK_NAMES[mask], n, n, L)
+        for i in range(h):
+            H, _ = oracle.attention(f64(Q[b, i]), f64(K[b, i]), f64(V[b, i]), c, allowed, rows)
+            ref[b, :, i * d_vh:(i + 1) * d_vh] = H
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref) <= 1e-2
+
+
+# ---------------------------------------------------------------------------
+# Statements of the pages checked on the GPU
+# ---------------------------------------------------------------------------
+
+def test_zero_output_projection_gives_exact_zero():
+    w = workloads.WORKLOADS[1].with_(B=1, n_q=256, n_k=256)
+    inp = workloads.make_inputs(w)
+    inp["W_O"] = torch.zeros_like(inp["W_O"])
+    assert torch.count_nonzero(run(w, inp)).item() == 0
+
+
+def test_batch_items_are_independent():
+    w = workloads.WORKLOADS[2].with_(B=3, n_q=256, n_k=256)
+    inp = workloads.make_inputs(w)
+    Y1 = run(w, inp).clone()
+    inp2 = dict(inp)
+    inp2["X_q"] = inp["X_q"].clone()
+    inp2["X_q"][1] = -inp2["X_q"][1]
+    Y2 = run(w, inp2)
+    assert torch.equal(Y1[0], Y2[0]) and torch.equal(Y1[2], Y2[2])
+    assert not torch.equal(Y1[1], Y2[1])
+
+
+def test_head_permutation_with_matching_w_o_blocks():
+    w = workloads.WORKLOADS[1].with_(B=1, n_q=256, n_k=256, d_model=256, h=4, d_o=256)
+    inp = workloads.make_inputs(w)
+    perm = [2, 0, 3, 1]
+    d = w.d_h
+    cols = lambda W: torch.cat([W[:, p * d:(p + 1) * d] for p in perm], dim=1)
+    inp2 = dict(inp, W_Q=cols(inp["W_Q"]), W_K=cols(inp["W_K"]), W_V=cols(inp["W_V"]),
+                W_O=torch.cat([inp["W_O"][p * d:(p + 1) * d] for p in perm], dim=0))
+    assert rel_err(f64(run(w, inp)), f64(run(w, inp2))) <= 1e-2
+
+
+def test_workspace_contents_on_entry_do_not_matter():
+    w = workloads.WORKLOADS[3].with_(B=2, n_q=300, n_k=300, d_model=256, h=2, d_o=256)
+    inp = workloads.make_inputs(w, lengths=[300, 131])
+    t = to_dev(inp)
+    nbytes = mha.workspace_size(w.B, w.n_q, w.n_k, w.d_model, w.h, w.d_h, w.d_vh, w.d_o, w.dtype)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN bit patterns
+    Y = mha.forward(t["X_q"], None, t["W_Q"], t["W_K"], t["W_V"], t["W_O"], w.h, w.d_h, w.d_vh,
+                    w.c, w.mask, inp["valid_len"], workspace=ws)
+    torch.cuda.synchronize()
+    check_full(w, inp, Y)
+
+
+# ---------------------------------------------------------------------------
+# Failure detection without a fault: a wait that nothing completes
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mha.selftest_wait_timeout(err, 2_000_000)  # 2 ms
+    torch.cuda.synchronize()
+    assert mha.get_device_error(err) == 6  # MHA_ERR_DEVICE_TIMEOUT
+    assert mha.get_device_error(err) == 0  # read resets the word
+    w = workloads.WORKLOADS[1].with_(B=1, n_q=128, n_k=128)
+    inp = workloads.make_inputs(w)
+    check_full(w, inp, run(w, inp))
