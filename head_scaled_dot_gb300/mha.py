@@ -85,7 +85,14 @@ def status_string(status):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device pointer of a tensor (or an int / c_void_p passed through)."""
+    if t is None:
+        return None
+    if isinstance(t, ctypes.c_void_p):
+        return t
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
