@@ -105,8 +105,9 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;            // [STAGES]
   uint64_t* v_full = k_full + C::STAGES;    // [STAGES]
-  uint64_t* kv_empty = v_full + C::STAGES;  // [STAGES]
-  uint64_t* s_full = kv_empty + C::STAGES;  // [2]
+  uint64_t* k_empty = v_full + C::STAGES;   // [STAGES] freed by S = Q K^T
+  uint64_t* v_empty = k_empty + C::STAGES;  // [STAGES] freed by z += P V
+  uint64_t* s_full = v_empty + C::STAGES;   // [2]
   uint64_t* p_full = s_full + 2;            // [2]
   uint64_t* o_full = p_full + 2;            // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
@@ -117,7 +118,8 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -147,22 +149,32 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
 #pragma unroll
       for (int p = 0; p < DQK / 64; ++p) tma_load_3d(q_s + p * 16384, &P.qmap, q_full, 64 * p, q0, bh);
       int kb = 0;
+      bool gave_up = false;
       for (; kb < nblk; ++kb) {
         const int s = kb % C::STAGES;
-        if (kb >= C::STAGES && !mbar_wait(&kv_empty[s], ((kb / C::STAGES) - 1) & 1, w)) break;
         uint8_t* k_s = kv_s + s * C::STAGE_BYTES;
         uint8_t* v_s = k_s + C::K_BYTES;
         const int k0 = kb * BLK_N;
+        const uint32_t reuse = ((kb / C::STAGES) - 1) & 1;
+        if (kb >= C::STAGES && !mbar_wait(&k_empty[s], reuse, w)) {
+          gave_up = true;
+          break;
+        }
         mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
 #pragma unroll
         for (int p = 0; p < DQK / 64; ++p)
           tma_load_3d(k_s + p * 16384, &P.kmap, &k_full[s], 64 * p, k0, bh);
+        if (kb >= C::STAGES && !mbar_wait(&v_empty[s], reuse, w)) {
+          ++kb;  // K of this block is in flight: drain it too
+          gave_up = true;
+          break;
+        }
         mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
 #pragma unroll
         for (int p = 0; p < DV / 64; ++p)
           tma_load_3d(v_s + p * 16384, &P.vmap, &v_full[s], 64 * p, k0, bh);
       }
-      if (kb < nblk) {  // gave up: let this CTA's loads land before it exits
+      if (gave_up) {  // let this CTA's loads land before it exits
         drain(q_full, 0);
         for (int k = (kb > C::STAGES ? kb - C::STAGES : 0); k < kb; ++k) {
           drain(&k_full[k % C::STAGES], (k / C::STAGES) & 1);
@@ -188,6 +200,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
           umma_ss(d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
                   idesc_qk, kk > 0);
         }
+        umma_commit(&k_empty[s]);  // this K stage can be refilled once S_kb is done
         umma_commit(&s_full[kb & 1]);
         return true;
       };
@@ -204,7 +217,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
           umma_ts(tmem + O_COL, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, 16384, 1024),
                   idesc_pv, (kb > 0 || kk > 0));
         }
-        umma_commit(&kv_empty[s]);
+        umma_commit(&v_empty[s]);
         umma_commit(o_full);
         return true;
       };
@@ -242,19 +255,12 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       tmem_wait_ld();
       const int k0 = kb * BLK_N;
       const bool masked = (k0 + BLK_N > L) || (P.causal && k0 + BLK_N - 1 > q0);
+      // allowed keys of this row in this block: k0 + c < lim
+      const int lim = masked ? (P.causal ? min(L, q + 1) : L) - k0 : BLK_N;
       float mx = -INFINITY;
-      if (masked) {
-        const int lim = P.causal ? min(L, q + 1) : L;  // allowed keys: j < lim
 #pragma unroll
-        for (int c = 0; c < BLK_N; ++c) {
-          const float v = (k0 + c < lim) ? __uint_as_float(sr[c]) : -INFINITY;
-          sr[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BLK_N; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-      }
+      for (int c = 0; c < BLK_N; ++c)
+        mx = fmaxf(mx, (!masked || c < lim) ? __uint_as_float(sr[c]) : -INFINITY);
       const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
       const float m_new = fmaxf(m_run, m_blk);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -263,11 +269,16 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       uint32_t pk[BLK_N / 2];
 #pragma unroll
       for (int c = 0; c < BLK_N; c += 4) {
-        // masked scores are -inf: 2^(-inf) = 0 exactly
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c + 0]), cl2, -m_use));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), cl2, -m_use));
-        const float p2 = ex2_approx(fmaf(__uint_as_float(sr[c + 2]), cl2, -m_use));
-        const float p3 = ex2_approx(fmaf(__uint_as_float(sr[c + 3]), cl2, -m_use));
+        float p0 = ex2_approx(fmaf(__uint_as_float(sr[c + 0]), cl2, -m_use));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), cl2, -m_use));
+        float p2 = ex2_approx(fmaf(__uint_as_float(sr[c + 2]), cl2, -m_use));
+        float p3 = ex2_approx(fmaf(__uint_as_float(sr[c + 3]), cl2, -m_use));
+        if (masked) {  // forbidden keys get weight exactly 0
+          p0 = (c + 0 < lim) ? p0 : 0.f;
+          p1 = (c + 1 < lim) ? p1 : 0.f;
+          p2 = (c + 2 < lim) ? p2 : 0.f;
+          p3 = (c + 3 < lim) ? p3 : 0.f;
+        }
         sum0 += p0;
         sum1 += p1;
         sum2 += p2;
