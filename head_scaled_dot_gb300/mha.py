@@ -33,6 +33,7 @@ EXPORTS = (
     "mha_workspace_size", "mha_workspace_layout", "mha_forward", "mha_qkv_projection", "mha_attention",
     "mha_output_projection", "mha_get_device_error", "mha_status_string",
     "mha_selftest_wait_timeout", "mha_kernel_launch_count", "mha_version",
+    "mha_forward_no_alloc",
 )
 
 _lib = None
@@ -60,6 +61,8 @@ def load(path=LIB_PATH):
     lib.mha_workspace_layout.argtypes = [I] * 6 + [I, ctypes.POINTER(S)]
     lib.mha_forward.restype = I
     lib.mha_forward.argtypes = [P] * 7 + [I] * 8 + [F, I, P, I, P, S, P]
+    lib.mha_forward_no_alloc.restype = I
+    lib.mha_forward_no_alloc.argtypes = [P] * 7 + [I] * 8 + [F, I, P, I, P]
     lib.mha_qkv_projection.restype = I
     lib.mha_qkv_projection.argtypes = [P] * 8 + [I] * 7 + [I, P, P]
     lib.mha_attention.restype = I
@@ -155,6 +158,30 @@ def forward(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, mask="none", valid_l
     _check(st, "mha_forward")
     if check:
         _check(lib.mha_get_device_error(_ptr(workspace), _stream(stream)), "mha_forward (device)")
+    return out
+
+
+NO_ALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def forward_no_alloc(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, mask="none",
+                     valid_len=None, out=None, stream=None):
+    """mha_forward_no_alloc: the forward pass with the library's own fixed
+    32 MiB device scratch instead of a workspace (for callers that cannot
+    allocate). `out` (B, n_q, d_o) is the only buffer the caller provides."""
+    lib = load()
+    B, n_q, d_model = X_q.shape
+    n_k = n_q if X_kv is None else X_kv.shape[1]
+    d_o = W_O.shape[1]
+    dt = TORCH_DTYPES[X_q.dtype]
+    if out is None:
+        out = torch.empty((B, n_q, d_o), dtype=X_q.dtype, device=X_q.device)
+    lens, keep = _lens(valid_len, B)
+    st = lib.mha_forward_no_alloc(_ptr(X_q), _ptr(X_kv), _ptr(W_Q), _ptr(W_K), _ptr(W_V),
+                                  _ptr(W_O), _ptr(out), B, n_q, n_k, d_model, h, d_h, d_vh, d_o,
+                                  float(c), MASKS[mask], lens, DTYPES[dt], _stream(stream))
+    del keep
+    _check(st, "mha_forward_no_alloc")
     return out
 
 

@@ -181,6 +181,44 @@ MHA_API mha_status mha_output_projection(const void* Z, const void* W_O, void* Y
                                  mha_dtype dt, int32_t* dev_error,
                                  void* stream);
 
+/* Size of the device scratch built into the library for mha_forward_no_alloc. */
+#define MHA_NO_ALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * mha_forward without a workspace, for callers that cannot allocate device
+ * memory: code running where cudaMalloc is forbidden or unavailable, such as
+ * inside a host framework that owns every device allocation, a plugin held
+ * to a fixed memory budget, or a loop that must not allocate once running.
+ * The caller passes its inputs and outputs exactly as for mha_forward; the
+ * intermediates (head-split Q, K, V, the concatenated Z and the device error
+ * word) live in a static device array of MHA_NO_ALLOC_SCRATCH_BYTES (32 MiB)
+ * that is part of the library. The pages define no such entry point: it has
+ * no counterpart there.
+ *
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   Every GPU on which the library's device code is loaded holds the 32 MiB
+ *   until the process exits.
+ * - Sizes whose intermediates need more than MHA_NO_ALLOC_SCRATCH_BYTES
+ *   (mha_workspace_size(...) > 32 MiB) return MHA_ERR_WORKSPACE before any
+ *   CUDA call. Other arguments are checked as in mha_forward.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current, and caches it; make that
+ *   first call before any stream capture on that device.
+ * - Every call shares the one array and leaves its contents behind; the error
+ *   word is reset at the start of each call. Calls whose work overlaps on the
+ *   GPU (different streams, or other host threads) race on the array: order
+ *   them on one stream or synchronise between them.
+ * - A kernel that gives up on a barrier records the timeout in the array's
+ *   error word, which this entry point does not read back; a caller that needs
+ *   that report uses mha_forward and mha_get_device_error.
+ */
+MHA_API mha_status mha_forward_no_alloc(const void* X_q, const void* X_kv, const void* W_Q,
+                                        const void* W_K, const void* W_V, const void* W_O,
+                                        void* Y, int B, int n_q, int n_k, int d_model, int h,
+                                        int d_h, int d_vh, int d_o, float c,
+                                        mha_mask_kind mask, const int32_t* valid_len,
+                                        mha_dtype dt, void* stream);
+
 /*
  * Reads the device error word (the workspace base for mha_forward, or the
  * dev_error given to a step), waits for `stream`, resets the word to 0 and
