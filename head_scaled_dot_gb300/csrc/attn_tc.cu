@@ -1,27 +1,37 @@
 // attn_tc.cu - fused masked attention on tcgen05 tensor cores (bf16).
 //
-// For one (batch item b, head i, 128-row query tile) a CTA folds the allowed
-// keys block by block into the stable summary of every query row ("Stable
-// summary of an attention key block", Definition, alphabetamath.cc):
-//   m = max_j s_ij,  l = sum_j e^{s_ij - m},  z = sum_j e^{s_ij - m} v_j
-// merging each 128-key block's summary into the running one with
+// A CTA takes two 128-row query tiles of one (batch item b, head i) and folds
+// the allowed keys, 128 at a time, into the stable summary of every query row
+// ("Stable summary of an attention key block", Definition, alphabetamath.cc):
+//   m = max_j s_ij,  l = sum_j e^{s_ij - m},  z = sum_j e^{s_ij - m} v_j,
+// merging each block into the running summary with
 //   m' = max(m, m_blk),  l' = e^{m - m'} l + e^{m_blk - m'} l_blk,  z' likewise,
 // and writes z / l once per row. The n_q x n_k score matrix only ever exists
-// one 128 x 128 block at a time, in tensor memory.
+// as one 128 x 128 block per tile, in tensor memory (TMEM).
 //
-// Roles (192 threads):
-//   warp 0      TMA producer: Q once, then K and V blocks into a STAGES ring
-//   warp 1      MMA issuer: S_j = Q K_j^T (SMEM x SMEM -> TMEM), then
-//               z += P_j V_j (P from TMEM, V from SMEM -> TMEM accumulator O)
-//   warps 2..5  softmax: thread = query row = TMEM lane. Loads its row of S_j,
-//               takes the row max in-thread (no shuffles: a TMEM lane holds a
-//               whole row), computes p = 2^{c log2(e) s - m}, its sum, writes p
-//               as bf16 into the columns of S_j (P aliases S), and rescales its
-//               row of O by e^{m - m'} only when its max grew. At the end:
-//               O / l -> bf16 -> Z in the concatenated (B, n_q, h*d_vh) layout.
-// S is double-buffered in TMEM so S_{j+1} = Q K_{j+1}^T runs while the
-// softmax works on S_j. Fully masked key blocks (past the diagonal, past the
-// valid length) are never loaded: they are the empty summary.
+// Roles (384 threads, three warpgroups):
+//   warp 0        TMA producer: both Q tiles once, then K and V blocks into a
+//                 STAGES-deep ring (K and V freed separately)
+//   warp 1        MMA issuer: S_t = Q_t K_j^T (SMEM x SMEM -> TMEM) and
+//                 z_t += P_t V_j (P from TMEM, V from SMEM) for tiles t = 0, 1,
+//                 interleaved so that one tile's softmax overlaps the other
+//                 tile's MMAs
+//   warps 4..7    softmax of tile 0, warps 8..11 softmax of tile 1: thread =
+//                 query row = TMEM lane. It loads its row of S, takes the row
+//                 max in-thread (a TMEM lane holds a whole row: no shuffles),
+//                 computes p = 2^{c log2(e) s - m}, writes p as bf16 over the
+//                 columns of S (P aliases S), and at the end writes z / l in
+//                 the concatenated (B, n_q, h*d_vh) layout.
+//
+// Stale maximum: the running m of a row is only raised when a block's max
+// exceeds it by more than 2^8 (then z and l are rescaled by e^{m - m'} in
+// TMEM). Otherwise the block is summarised against the old m: its terms are
+// e^{s - m} <= 2^8, and z / l is unchanged because a common factor e^{-m}
+// cancels between z and l. This keeps the rescale (which must wait for the
+// previous z += P V) off the common path.
+//
+// Key blocks that are fully masked (past the causal diagonal, past the valid
+// length) are never loaded: they are the empty summary.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -31,9 +41,11 @@
 namespace mha {
 namespace {
 
-constexpr int BLK_M = 128;  // query rows per CTA
+constexpr int BLK_M = 128;  // query rows per tile (two tiles per CTA)
 constexpr int BLK_N = 128;  // keys per block
-constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL = 256, TMEM_COLS = 512;
+constexpr int NTHREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_LOG2 = 8.0f;  // raise m only when the max grows by > 2^8
 
 struct AttnTcParams {
   CUtensorMap qmap;  // Q: dims {d_h, n_q, B*h}, box {64, 128, 1}
@@ -51,12 +63,18 @@ struct AttnTcParams {
 
 template <int DQK, int DV>
 struct ACfg {
-  static constexpr int Q_BYTES = BLK_M * DQK * 2;
+  static constexpr int Q_TILE_BYTES = BLK_M * DQK * 2;
   static constexpr int K_BYTES = BLK_N * DQK * 2;
   static constexpr int V_BYTES = BLK_N * DV * 2;
-  static constexpr int STAGES = (DQK + DV) <= 192 ? 3 : 2;
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-  static constexpr int SMEM = Q_BYTES + STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int BUDGET = 227 * 1024 - 2 * Q_TILE_BYTES - 1024 - 512;
+  static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 4 ? 4 : (BUDGET / STAGE_BYTES);
+  static constexpr int SMEM = 2 * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + 512;
+  // TMEM columns: S of tile 0 and 1, then z (O) of tile 0 and 1.
+  static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
+  static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + DV;
+  static_assert(STAGES >= 2, "shared memory");
+  static_assert(256 + 2 * DV <= TMEM_COLS, "tensor memory");
 };
 
 __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
@@ -67,30 +85,46 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Number of 128-key blocks a tile starting at row tq0 must fold (0 when all
+// its rows are padding).
+__device__ __forceinline__ int tile_blocks(const AttnTcParams& P, int tq0, int L, int q_end) {
+  if (tq0 >= q_end) return 0;
+  int k_end = L;
+  if (P.causal) k_end = min(k_end, tq0 + BLK_M);
+  return (k_end + BLK_N - 1) / BLK_N;
+}
+
 template <int DQK, int DV>
-__global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
+__global__ void __launch_bounds__(NTHREADS, 1)
+    attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
   using C = ACfg<DQK, DV>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_qt = gridDim.x;
-  // causal: heavy tiles (large q0) first, so the light ones fill the tail
-  const int qt = P.causal ? (n_qt - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int q0 = qt * BLK_M;
+  const int npair = gridDim.x;
+  // causal: heavy tile pairs (large q0) first, so the light ones fill the tail
+  const int pi = P.causal ? (npair - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int q0 = pi * 2 * BLK_M;
   const int head = blockIdx.y, b = blockIdx.z;
   const int L = P.padding ? P.valid_len[b] : P.n_k;
   const int q_end = P.pad_queries ? min(L, P.n_q) : P.n_q;
-  int k_end = L;
-  if (P.causal) k_end = min(k_end, q0 + BLK_M);
-  const int nblk = (q0 < q_end) ? (k_end + BLK_N - 1) / BLK_N : 0;
+  const int nb0 = tile_blocks(P, q0, L, q_end);
+  const int nb1 = (q0 + BLK_M < P.n_q) ? tile_blocks(P, q0 + BLK_M, L, q_end) : 0;
+  const int nmax = nb1 > nb0 ? nb1 : nb0;  // tile 0's blocks are a prefix of tile 1's
   __nv_bfloat16* Zg = static_cast<__nv_bfloat16*>(P.Z);
   const long long zrow_stride = (long long)P.h * DV;
   const long long zbase = (long long)b * P.n_q * zrow_stride + (long long)head * DV;
 
-  if (nblk == 0) {
-    // every row of this tile is padding: Z rows are exact zeros
-    const int rows = min(BLK_M, P.n_q - q0);
-    for (int e = threadIdx.x; e < rows * (DV / 8); e += blockDim.x) {
-      const int r = e / (DV / 8), c8 = e % (DV / 8);
-      *reinterpret_cast<uint4*>(Zg + zbase + (long long)(q0 + r) * zrow_stride + c8 * 8) =
+  if (nmax == 0) {
+    // every row of both tiles is padding: Z rows are exact zeros
+    const int r1 = min(q0 + 2 * BLK_M, P.n_q);
+    for (int e = threadIdx.x; e < (r1 - q0) * (DV / 8); e += NTHREADS) {
+      const int r = q0 + e / (DV / 8), c8 = e % (DV / 8);
+      *reinterpret_cast<uint4*>(Zg + zbase + (long long)r * zrow_stride + c8 * 8) =
           make_uint4(0, 0, 0, 0);
     }
     return;
@@ -99,18 +133,18 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* q_s = smem;
-  uint8_t* kv_s = smem + C::Q_BYTES;
+  uint8_t* q_s = smem;  // two Q tiles
+  uint8_t* kv_s = smem + 2 * C::Q_TILE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + C::STAGES * C::STAGE_BYTES);
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;            // [STAGES]
   uint64_t* v_full = k_full + C::STAGES;    // [STAGES]
-  uint64_t* k_empty = v_full + C::STAGES;   // [STAGES] freed by S = Q K^T
-  uint64_t* v_empty = k_empty + C::STAGES;  // [STAGES] freed by z += P V
-  uint64_t* s_full = v_empty + C::STAGES;   // [2]
-  uint64_t* p_full = s_full + 2;            // [2]
-  uint64_t* o_full = p_full + 2;            // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
+  uint64_t* k_empty = v_full + C::STAGES;   // [STAGES] freed once S of both tiles is done
+  uint64_t* v_empty = k_empty + C::STAGES;  // [STAGES] freed once both z += P V are done
+  uint64_t* s_full = v_empty + C::STAGES;   // [2] per tile
+  uint64_t* p_full = s_full + 2;            // [2] per tile
+  uint64_t* o_full = p_full + 2;            // [2] per tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
@@ -121,11 +155,11 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);  // one arrival per softmax warp
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);  // one arrival per softmax warp of the tile
+      mbar_init(&o_full[t], 1);
     }
-    mbar_init(o_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -140,17 +174,23 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
   const WaitCtl w{P.err, abort_flag, P.limit_ns};
   const int bh = b * P.h + head;
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < 4) {
+    // Warpgroup 0: producer and MMA issuer need few registers.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+    if (warp == 0 && lane == 0) {
       tma_prefetch_desc(&P.qmap);
       tma_prefetch_desc(&P.kmap);
       tma_prefetch_desc(&P.vmap);
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      const int ntiles = nb1 > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, ntiles * C::Q_TILE_BYTES);
+      for (int t = 0; t < ntiles; ++t)
 #pragma unroll
-      for (int p = 0; p < DQK / 64; ++p) tma_load_3d(q_s + p * 16384, &P.qmap, q_full, 64 * p, q0, bh);
+        for (int p = 0; p < DQK / 64; ++p)
+          tma_load_3d(q_s + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, q_full, 64 * p,
+                      q0 + t * BLK_M, bh);
       int kb = 0;
       bool gave_up = false;
-      for (; kb < nblk; ++kb) {
+      for (; kb < nmax; ++kb) {
         const int s = kb % C::STAGES;
         uint8_t* k_s = kv_s + s * C::STAGE_BYTES;
         uint8_t* v_s = k_s + C::K_BYTES;
@@ -165,7 +205,7 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
         for (int p = 0; p < DQK / 64; ++p)
           tma_load_3d(k_s + p * 16384, &P.kmap, &k_full[s], 64 * p, k0, bh);
         if (kb >= C::STAGES && !mbar_wait(&v_empty[s], reuse, w)) {
-          ++kb;  // K of this block is in flight: drain it too
+          ++kb;
           gave_up = true;
           break;
         }
@@ -181,50 +221,72 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
           drain(&v_full[k % C::STAGES], (k / C::STAGES) & 1);
         }
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16_f32(BLK_M, BLK_N, 0, 0) | (P.negate ? (1u << 13) : 0u);
+    } else if (warp == 1 && lane == 0) {
+      const uint32_t idesc_qk =
+          idesc_bf16_f32(BLK_M, BLK_N, 0, 0) | (P.negate ? (1u << 13) : 0u);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BLK_M, DV, 0, 1);
       const uint32_t q_addr = smem_u32(q_s);
       bool ok = mbar_wait(q_full, 0, w);
-      auto issue_s = [&](int kb) -> bool {
-        const int s = kb % C::STAGES;
-        if (!mbar_wait(&k_full[s], (kb / C::STAGES) & 1, w)) return false;
+      auto wait_k = [&](int kb) -> bool {
+        if (!mbar_wait(&k_full[kb % C::STAGES], (kb / C::STAGES) & 1, w)) return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(kv_s + s * C::STAGE_BYTES);
-        const uint32_t d = tmem + ((kb & 1) ? S_COL1 : S_COL0);
+        return true;
+      };
+      auto issue_s = [&](int t, int kb) {
+        const uint32_t k_addr = smem_u32(kv_s + (kb % C::STAGES) * C::STAGE_BYTES);
+        const uint32_t qa = q_addr + t * C::Q_TILE_BYTES;
+        const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          umma_ss(d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+          umma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
                   idesc_qk, kk > 0);
         }
-        umma_commit(&k_empty[s]);  // this K stage can be refilled once S_kb is done
-        umma_commit(&s_full[kb & 1]);
-        return true;
+        umma_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int kb) -> bool {
-        const int s = kb % C::STAGES;
-        if (!mbar_wait(&p_full[kb & 1], (kb >> 1) & 1, w)) return false;
-        if (!mbar_wait(&v_full[s], (kb / C::STAGES) & 1, w)) return false;
+      auto issue_pv = [&](int t, int kb) -> bool {
+        if (!mbar_wait(&p_full[t], kb & 1, w)) return false;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(kv_s + s * C::STAGE_BYTES + C::K_BYTES);
-        const uint32_t p_tmem = tmem + ((kb & 1) ? S_COL1 : S_COL0);
+        const uint32_t v_addr =
+            smem_u32(kv_s + (kb % C::STAGES) * C::STAGE_BYTES + C::K_BYTES);
+        const uint32_t p_tmem = tmem + (t ? C::S_COL1 : C::S_COL0);
+        const uint32_t o_tmem = tmem + (t ? C::O_COL1 : C::O_COL0);
 #pragma unroll
         for (int kk = 0; kk < BLK_N / 16; ++kk) {
           // V is MN-major: 16 key rows of 128 B; 64-column panels 16 KB apart.
-          umma_ts(tmem + O_COL, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, 16384, 1024),
+          umma_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, 16384, 1024),
                   idesc_pv, (kb > 0 || kk > 0));
         }
-        umma_commit(&v_empty[s]);
-        umma_commit(o_full);
+        umma_commit(&o_full[t]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int kb = 0; kb < nblk && ok; ++kb) {
-        if (kb + 1 < nblk) ok = issue_s(kb + 1);
-        if (ok) ok = issue_pv(kb);
+      // prologue: S of block 0 for both tiles
+      if (ok) ok = wait_k(0);
+      if (ok) {
+        if (nb0 > 0) issue_s(0, 0);
+        if (nb1 > 0) issue_s(1, 0);
+        umma_commit(&k_empty[0]);
+      }
+      for (int kb = 0; kb < nmax && ok; ++kb) {
+        const int s = kb % C::STAGES;
+        if (!mbar_wait(&v_full[s], (kb / C::STAGES) & 1, w)) {
+          ok = false;
+          break;
+        }
+        const bool next = kb + 1 < nmax;
+        bool k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int nbt = t ? nb1 : nb0;
+          if (kb < nbt) ok = issue_pv(t, kb);
+          if (ok && next && kb + 1 < nbt) {
+            // S_t of the next block overwrites P_t of this one: issued after it
+            if (!k_ready) ok = k_ready = wait_k(kb + 1);
+            if (ok) issue_s(t, kb + 1);
+          }
+        }
+        if (!ok) break;
+        umma_commit(&v_empty[s]);
+        if (next) umma_commit(&k_empty[(kb + 1) % C::STAGES]);
       }
       if (!ok) {  // gave up: wait for this thread's MMAs before TMEM is released
         umma_commit(&s_full[0]);
@@ -233,80 +295,106 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       }
     }
   } else {
-    // Softmax warps: warp w owns TMEM lanes (query rows) 32*(w%4) .. +31.
-    const int g = warp & 3;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+    const int t = (warp - 4) / 4;  // tile of this warpgroup
+    const int g = warp & 3;        // TMEM lane slice 32*g .. 32*g+31
     const int r = 32 * g + lane;
-    const int q = q0 + r;
+    const int tq0 = q0 + t * BLK_M;
+    const int q = tq0 + r;
+    const int nblk = t ? nb1 : nb0;
     const uint32_t lane_off = static_cast<uint32_t>(32 * g) << 16;
+    const uint32_t s_addr = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
+    const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
     const float cl2 = P.cl2;
+    const float2 cl2x2 = make_float2(cl2, cl2);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int kb = 0; kb < nblk; ++kb) {
-      if (!mbar_wait(&s_full[kb & 1], (kb >> 1) & 1, w)) {
+      if (!mbar_wait(&s_full[t], kb & 1, w)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t s_addr = tmem + lane_off + ((kb & 1) ? S_COL1 : S_COL0);
       uint32_t sr[BLK_N];
 #pragma unroll
       for (int c = 0; c < BLK_N / 32; ++c)
         tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
       tmem_wait_ld();
       const int k0 = kb * BLK_N;
-      const bool masked = (k0 + BLK_N > L) || (P.causal && k0 + BLK_N - 1 > q0);
+      const bool masked = (k0 + BLK_N > L) || (P.causal && k0 + BLK_N - 1 > tq0);
       // allowed keys of this row in this block: k0 + c < lim
       const int lim = masked ? (P.causal ? min(L, q + 1) : L) - k0 : BLK_N;
-      float mx = -INFINITY;
+      if (masked) {
 #pragma unroll
-      for (int c = 0; c < BLK_N; ++c)
-        mx = fmaxf(mx, (!masked || c < lim) ? __uint_as_float(sr[c]) : -INFINITY);
-      const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
-      const float m_new = fmaxf(m_run, m_blk);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run - m_use);  // e^{m - m'}; 0 when m = -inf
-      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-      uint32_t pk[BLK_N / 2];
+        for (int c = 0; c < BLK_N; ++c)
+          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int c = 0; c < BLK_N; c += 4) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(sr[c + 0]), cl2, -m_use));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), cl2, -m_use));
-        float p2 = ex2_approx(fmaf(__uint_as_float(sr[c + 2]), cl2, -m_use));
-        float p3 = ex2_approx(fmaf(__uint_as_float(sr[c + 3]), cl2, -m_use));
-        if (masked) {  // forbidden keys get weight exactly 0
-          p0 = (c + 0 < lim) ? p0 : 0.f;
-          p1 = (c + 1 < lim) ? p1 : 0.f;
-          p2 = (c + 2 < lim) ? p2 : 0.f;
-          p3 = (c + 3 < lim) ? p3 : 0.f;
-        }
-        sum0 += p0;
-        sum1 += p1;
-        sum2 += p2;
-        sum3 += p3;
-        pk[c / 2] = pack_bf16x2(p0, p1);
-        pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+        mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+        mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
       }
-      l_run = l_run * alpha + ((sum0 + sum1) + (sum2 + sum3));
-      // P_j overwrites the first BLK_N/2 columns of S_j (two bf16 per column)
-      tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      // merge into the running summary: rescale this row of O by e^{m - m'}
-      // when its max grew (O must hold every earlier block first)
-      const bool grow = kb > 0 && m_new > m_run;
-      if (__any_sync(0xffffffffu, grow)) {
-        if (!mbar_wait(o_full, (kb - 1) & 1, w)) {
+      const float mx = fmaxf(mx0, mx1);
+      const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
+      // raise the running max only past the threshold (or on the first block)
+      const bool raise = (m_run == -INFINITY) ? true : (m_blk > m_run + RESCALE_LOG2);
+      const float m_new = raise ? fmaxf(m_run, m_blk) : m_run;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m_run - m_use);  // e^{m - m'}: 1 when m is kept
+      float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
+      const float2 negm = make_float2(-m_use, -m_use);
+      // P overwrites the first BLK_N/2 columns of S (two bf16 per column),
+      // written in two halves to keep fewer values live
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[BLK_N / 4];
+#pragma unroll
+        for (int cc = 0; cc < BLK_N / 2; cc += 4) {
+          const int c = h * (BLK_N / 2) + cc;
+          float2 x0 = __ffma2_rn(
+              make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cl2x2, negm);
+          float2 x1 = __ffma2_rn(
+              make_float2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), cl2x2, negm);
+          x0.x = ex2_approx(x0.x);
+          x0.y = ex2_approx(x0.y);
+          x1.x = ex2_approx(x1.x);
+          x1.y = ex2_approx(x1.y);
+          if (masked) {  // forbidden keys get weight exactly 0 (also when c = 0)
+            if (c + 0 >= lim) x0.x = 0.f;
+            if (c + 1 >= lim) x0.y = 0.f;
+            if (c + 2 >= lim) x1.x = 0.f;
+            if (c + 3 >= lim) x1.y = 0.f;
+          }
+          sum = __fadd2_rn(sum, x0);
+          sum_b = __fadd2_rn(sum_b, x1);
+          pk[cc / 2] = pack_bf16x2(x0.x, x0.y);
+          pk[cc / 2 + 1] = pack_bf16x2(x1.x, x1.y);
+        }
+        tmem_st32(s_addr + 32 * h, pk);
+      }
+      l_run = l_run * alpha + ((sum.x + sum.y) + (sum_b.x + sum_b.y));
+      // merge: rescale this row of z by e^{m - m'} when m was raised; z must
+      // already hold every earlier block (wait for the previous z += P V)
+      if (__any_sync(0xffffffffu, kb > 0 && raise)) {
+        if (!mbar_wait(&o_full[t], (kb - 1) & 1, w)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t o_addr = tmem + lane_off + O_COL;
 #pragma unroll
         for (int c = 0; c < DV / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(o_addr + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          for (int j = 0; j < 32; j += 2) {
+            const float2 v = __fmul2_rn(
+                make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
+                make_float2(alpha, alpha));
+            o[j] = __float_as_uint(v.x);
+            o[j + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(o_addr + 32 * c, o);
         }
       }
@@ -314,13 +402,19 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const __grid_constant__
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[kb & 1]);
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    if (ok && mbar_wait(o_full, (nblk - 1) & 1, w)) {
+    if (nblk == 0) {
+      // the whole tile is padding (tile 1 only): its rows are zero
+      if (q < P.n_q) {
+        uint4* dst = reinterpret_cast<uint4*>(Zg + zbase + (long long)q * zrow_stride);
+#pragma unroll
+        for (int j = 0; j < DV / 8; ++j) dst[j] = make_uint4(0, 0, 0, 0);
+      }
+    } else if (ok && mbar_wait(&o_full[t], (nblk - 1) & 1, w)) {
       tc_fence_after();
       const bool computed = q < q_end;
       const float inv = computed ? 1.f / l_run : 0.f;
-      const uint32_t o_addr = tmem + lane_off + O_COL;
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
@@ -360,8 +454,8 @@ mha_status launch(const AttnTcParams& P, int B, int h, int n_q, cudaStream_t s) 
       return MHA_ERR_CUDA;
     attr = true;
   }
-  const dim3 grid((n_q + BLK_M - 1) / BLK_M, h, B);
-  attn_tc_kernel<DQK, DV><<<grid, 192, C::SMEM, s>>>(P);
+  const dim3 grid((n_q + 2 * BLK_M - 1) / (2 * BLK_M), h, B);
+  attn_tc_kernel<DQK, DV><<<grid, NTHREADS, C::SMEM, s>>>(P);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }

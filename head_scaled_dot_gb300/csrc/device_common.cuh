@@ -73,7 +73,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // false (and records MHA_ERR_DEVICE_TIMEOUT) after w.limit_ns, or at once when
 // another role of the CTA has already given up. Never spins without bound:
 // the iteration count is capped as well as the time.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+static __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1; it != 0; ++it) {  // wraps after 2^32 polls at most
     if (mbar_try_wait(bar, parity)) return true;
