@@ -10,8 +10,10 @@
 // as one 128 x 128 block per tile, in tensor memory (TMEM).
 //
 // Roles (384 threads, three warpgroups):
-//   warp 0        TMA producer: both Q tiles once, then K and V blocks into a
-//                 STAGES-deep ring (K and V freed separately)
+//   warps 0, 2    TMA producers: warp 0 loads both Q tiles once and the K
+//                 blocks, warp 2 the V blocks, into a STAGES-deep ring (K and
+//                 V freed separately); each also prefetches the blocks a few
+//                 steps ahead into L2
 //   warp 1        MMA issuer: S_t = Q_t K_j^T (SMEM x SMEM -> TMEM) and
 //                 z_t += P_t V_j (P from TMEM, V from SMEM) for tiles t = 0, 1,
 //                 interleaved so that one tile's softmax overlaps the other
@@ -46,6 +48,7 @@ constexpr int BLK_N = 128;  // keys per block
 constexpr int NTHREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;  // raise m only when the max grows by > 2^8
+constexpr int PREFETCH = 4;           // K/V blocks requested into L2 ahead of the ring
 
 struct AttnTcParams {
   CUtensorMap qmap;  // Q: dims {d_h, n_q, B*h}, box {64, 128, 1}
@@ -176,50 +179,50 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp < 4) {
     // Warpgroup 0: producer and MMA issuer need few registers.
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
-    if (warp == 0 && lane == 0) {
-      tma_prefetch_desc(&P.qmap);
-      tma_prefetch_desc(&P.kmap);
-      tma_prefetch_desc(&P.vmap);
-      const int ntiles = nb1 > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, ntiles * C::Q_TILE_BYTES);
-      for (int t = 0; t < ntiles; ++t)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if ((warp == 0 || warp == 2) && lane == 0) {
+      // warp 0 streams Q and the K blocks, warp 2 the V blocks; each also asks
+      // L2 for the blocks PREFETCH ahead so that refills of the ring come
+      // from L2 rather than DRAM
+      const bool is_k = warp == 0;
+      const CUtensorMap* map = is_k ? &P.kmap : &P.vmap;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      const int panels = is_k ? DQK / 64 : DV / 64;
+      const uint32_t bytes = is_k ? C::K_BYTES : C::V_BYTES;
+      tma_prefetch_desc(map);
+      if (is_k) {
+        tma_prefetch_desc(&P.qmap);
+        const int ntiles = nb1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(q_full, ntiles * C::Q_TILE_BYTES);
+        for (int t = 0; t < ntiles; ++t)
 #pragma unroll
-        for (int p = 0; p < DQK / 64; ++p)
-          tma_load_3d(q_s + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, q_full, 64 * p,
-                      q0 + t * BLK_M, bh);
+          for (int p = 0; p < DQK / 64; ++p)
+            tma_load_3d(q_s + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, q_full, 64 * p,
+                        q0 + t * BLK_M, bh);
+      }
+      for (int kb = C::STAGES; kb < C::STAGES + PREFETCH && kb < nmax; ++kb)
+        for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, kb * BLK_N, bh);
       int kb = 0;
       bool gave_up = false;
       for (; kb < nmax; ++kb) {
         const int s = kb % C::STAGES;
-        uint8_t* k_s = kv_s + s * C::STAGE_BYTES;
-        uint8_t* v_s = k_s + C::K_BYTES;
-        const int k0 = kb * BLK_N;
-        const uint32_t reuse = ((kb / C::STAGES) - 1) & 1;
-        if (kb >= C::STAGES && !mbar_wait(&k_empty[s], reuse, w)) {
+        uint8_t* dst = kv_s + s * C::STAGE_BYTES + (is_k ? 0 : C::K_BYTES);
+        if (kb >= C::STAGES && !mbar_wait(&empty[s], ((kb / C::STAGES) - 1) & 1, w)) {
           gave_up = true;
           break;
         }
-        mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
-#pragma unroll
-        for (int p = 0; p < DQK / 64; ++p)
-          tma_load_3d(k_s + p * 16384, &P.kmap, &k_full[s], 64 * p, k0, bh);
-        if (kb >= C::STAGES && !mbar_wait(&v_empty[s], reuse, w)) {
-          ++kb;
-          gave_up = true;
-          break;
-        }
-        mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
-#pragma unroll
-        for (int p = 0; p < DV / 64; ++p)
-          tma_load_3d(v_s + p * 16384, &P.vmap, &v_full[s], 64 * p, k0, bh);
+        mbar_arrive_expect_tx(&full[s], bytes);
+        for (int p = 0; p < panels; ++p)
+          tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, kb * BLK_N, bh);
+        const int ahead = kb + C::STAGES + PREFETCH;
+        if (ahead < nmax)
+          for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, ahead * BLK_N, bh);
       }
-      if (gave_up) {  // let this CTA's loads land before it exits
-        drain(q_full, 0);
-        for (int k = (kb > C::STAGES ? kb - C::STAGES : 0); k < kb; ++k) {
-          drain(&k_full[k % C::STAGES], (k / C::STAGES) & 1);
-          drain(&v_full[k % C::STAGES], (k / C::STAGES) & 1);
-        }
+      if (gave_up) {  // let this thread's loads land before the CTA exits
+        if (is_k) drain(q_full, 0);
+        for (int k = (kb > C::STAGES ? kb - C::STAGES : 0); k < kb; ++k)
+          drain(&full[k % C::STAGES], (k / C::STAGES) & 1);
       }
     } else if (warp == 1 && lane == 0) {
       const uint32_t idesc_qk =
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
     const int t = (warp - 4) / 4;  // tile of this warpgroup
     const int g = warp & 3;        // TMEM lane slice 32*g .. 32*g+31
     const int r = 32 * g + lane;
