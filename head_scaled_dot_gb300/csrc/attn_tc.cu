@@ -14,13 +14,14 @@
 //                 blocks, warp 2 the V blocks, into a STAGES-deep ring (K and
 //                 V freed separately); each also prefetches the blocks a few
 //                 steps ahead into L2
-//   warp 1        MMA issuer: S_t = Q_t K_j^T (SMEM x SMEM -> TMEM) and
-//                 z_t += P_t V_j (P from TMEM, V from SMEM) for tiles t = 0, 1,
-//                 interleaved so that one tile's softmax overlaps the other
-//                 tile's MMAs
+//   warps 1, 3    MMA issuers, one per tile t: S_t = Q_t K_j^T (SMEM x SMEM
+//                 -> TMEM) and z_t += P_t V_j (P from TMEM, V from SMEM); the
+//                 two tiles' streams interleave on the tensor pipe, so one
+//                 tile's softmax overlaps the other tile's MMAs
 //   warps 4..7    softmax of tile 0, warps 8..11 softmax of tile 1: thread =
-//                 query row = TMEM lane. It loads its row of S, takes the row
-//                 max in-thread (a TMEM lane holds a whole row: no shuffles),
+//                 query row = TMEM lane. It reads its row of S from TMEM, takes
+//                 the row max in-thread (a TMEM lane holds a whole row: no
+//                 shuffles),
 //                 computes p = 2^{c log2(e) s - m}, writes p as bf16 over the
 //                 columns of S (P aliases S), and at the end writes z / l in
 //                 the concatenated (B, n_q, h*d_vh) layout.
@@ -155,8 +156,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&k_empty[s], nb1 > 0 ? 2 : 1);  // one arrival per active tile
+      mbar_init(&v_empty[s], nb1 > 0 ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -178,8 +179,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int bh = b * P.h + head;
 
   if (warp < 4) {
-    // Warpgroup 0: producer and MMA issuer need few registers.
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
     if ((warp == 0 || warp == 2) && lane == 0) {
       // warp 0 streams Q and the K blocks, warp 2 the V blocks; each also asks
       // L2 for the blocks PREFETCH ahead so that refills of the ring come
@@ -224,81 +223,94 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int k = (kb > C::STAGES ? kb - C::STAGES : 0); k < kb; ++k)
           drain(&full[k % C::STAGES], (k / C::STAGES) & 1);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+      // Two MMA issuers, one per query tile (warp 1: tile 0, warp 3: tile 1).
+      // Each keeps its own short tensor-instruction queue filled, so the
+      // bookkeeping of one (barrier waits, commits) is covered by the other's
+      // queued MMAs. Within a tile the order S_j, P_j V_j, S_{j+1}, ... is kept
+      // by the single issuing thread (S_{j+1} overwrites P_j in TMEM).
+      const int t = warp == 1 ? 0 : 1;
+      const int nbt = t ? nb1 : nb0;
       const uint32_t idesc_qk =
           idesc_bf16_f32(BLK_M, BLK_N, 0, 0) | (P.negate ? (1u << 13) : 0u);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BLK_M, DV, 0, 1);
-      const uint32_t q_addr = smem_u32(q_s);
-      bool ok = mbar_wait(q_full, 0, w);
-      auto wait_k = [&](int kb) -> bool {
-        if (!mbar_wait(&k_full[kb % C::STAGES], (kb / C::STAGES) & 1, w)) return false;
-        tc_fence_after();
-        return true;
-      };
-      auto issue_s = [&](int t, int kb) {
-        const uint32_t k_addr = smem_u32(kv_s + (kb % C::STAGES) * C::STAGE_BYTES);
-        const uint32_t qa = q_addr + t * C::Q_TILE_BYTES;
-        const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
+      // Shared-memory descriptors are built once; each operand is a base
+      // descriptor plus a small constant (the start address sits in the low
+      // 14 bits and every shared address is below 256 KB).
+      const uint64_t qd = sdesc_sw128(smem_u32(q_s + t * C::Q_TILE_BYTES), 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(smem_u32(kv_s), 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(smem_u32(kv_s + C::K_BYTES), 16384, 1024);
+      constexpr uint64_t STAGE_D = C::STAGE_BYTES >> 4;
+      const uint32_t s_tmem = tmem + (t ? C::S_COL1 : C::S_COL0);
+      const uint32_t o_tmem = tmem + (t ? C::O_COL1 : C::O_COL0);
+      auto issue_s = [&](int kb) {
+        const uint64_t kd = k_desc + (uint64_t)(kb % C::STAGES) * STAGE_D;
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          umma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                  idesc_qk, kk > 0);
+          // 16 elements = 32 B inside a 128 B swizzle row; 64-element panels 16 KB apart
+          const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+          umma_ss(s_tmem, qd + off, kd + off, idesc_qk, kk > 0);
         }
         umma_commit(&s_full[t]);
+        umma_commit(&k_empty[kb % C::STAGES]);  // this tile is done with K_kb
       };
-      auto issue_pv = [&](int t, int kb) -> bool {
-        if (!mbar_wait(&p_full[t], kb & 1, w)) return false;
-        tc_fence_after();
-        const uint32_t v_addr =
-            smem_u32(kv_s + (kb % C::STAGES) * C::STAGE_BYTES + C::K_BYTES);
-        const uint32_t p_tmem = tmem + (t ? C::S_COL1 : C::S_COL0);
-        const uint32_t o_tmem = tmem + (t ? C::O_COL1 : C::O_COL0);
+      auto issue_pv = [&](int kb) {
+        const uint64_t vd = v_desc + (uint64_t)(kb % C::STAGES) * STAGE_D;
 #pragma unroll
         for (int kk = 0; kk < BLK_N / 16; ++kk) {
-          // V is MN-major: 16 key rows of 128 B; 64-column panels 16 KB apart.
-          umma_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, 16384, 1024),
-                  idesc_pv, (kb > 0 || kk > 0));
+          // V is MN-major: 16 key rows of 128 B; 64-column panels 16 KB apart
+          umma_ts(o_tmem, s_tmem + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                  (kb > 0 || kk > 0));
         }
         umma_commit(&o_full[t]);
-        return true;
+        umma_commit(&v_empty[kb % C::STAGES]);  // this tile is done with V_kb
       };
-      // prologue: S of block 0 for both tiles
-      if (ok) ok = wait_k(0);
-      if (ok) {
-        if (nb0 > 0) issue_s(0, 0);
-        if (nb1 > 0) issue_s(1, 0);
-        umma_commit(&k_empty[0]);
-      }
-      for (int kb = 0; kb < nmax && ok; ++kb) {
-        const int s = kb % C::STAGES;
-        if (!mbar_wait(&v_full[s], (kb / C::STAGES) & 1, w)) {
-          ok = false;
-          break;
-        }
-        const bool next = kb + 1 < nmax;
-        bool k_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int nbt = t ? nb1 : nb0;
-          if (kb < nbt) ok = issue_pv(t, kb);
-          if (ok && next && kb + 1 < nbt) {
-            // S_t of the next block overwrites P_t of this one: issued after it
-            if (!k_ready) ok = k_ready = wait_k(kb + 1);
-            if (ok) issue_s(t, kb + 1);
+      bool ok = nbt > 0 && mbar_wait(q_full, 0, w);
+      int kb = 0;
+      if (ok && mbar_wait(&k_full[0], 0, w)) {
+        tc_fence_after();
+        issue_s(0);
+        for (; kb < nbt; ++kb) {
+          const int s = kb % C::STAGES;
+          if (!mbar_wait(&v_full[s], (kb / C::STAGES) & 1, w) ||
+              !mbar_wait(&p_full[t], kb & 1, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(kb);
+          if (kb + 1 < nbt) {
+            if (!mbar_wait(&k_full[(kb + 1) % C::STAGES], ((kb + 1) / C::STAGES) & 1, w)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(kb + 1);  // after P_kb V_kb in this thread's order
           }
         }
-        if (!ok) break;
-        umma_commit(&v_empty[s]);
-        if (next) umma_commit(&k_empty[(kb + 1) % C::STAGES]);
+      } else {
+        ok = nbt == 0;
       }
-      if (!ok) {  // gave up: wait for this thread's MMAs before TMEM is released
-        umma_commit(&s_full[0]);
-        drain(&s_full[0], 0);
-        drain(&s_full[0], 1);
+      // Causal tile 0 needs fewer blocks than tile 1; it still releases the
+      // remaining K/V stages, each once that block's data is in (so the
+      // arrival lands in that block's phase of the empty barrier).
+      if (ok && nbt > 0) {
+        for (int k2 = nbt; k2 < nmax; ++k2) {
+          const int s = k2 % C::STAGES;
+          const uint32_t par = (k2 / C::STAGES) & 1;
+          if (!mbar_wait(&k_full[s], par, w)) break;
+          mbar_arrive(&k_empty[s]);
+          if (!mbar_wait(&v_full[s], par, w)) break;
+          mbar_arrive(&v_empty[s]);
+        }
+      }
+      if (!ok && nbt > 0) {  // gave up: wait for this thread's MMAs before TMEM is released
+        umma_commit(&s_full[t]);
+        drain(&s_full[t], 0);
+        drain(&s_full[t], 1);
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
     const int t = (warp - 4) / 4;  // tile of this warpgroup
     const int g = warp & 3;        // TMEM lane slice 32*g .. 32*g+31
     const int r = 32 * g + lane;
@@ -318,25 +330,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sr[BLK_N];
-#pragma unroll
-      for (int c = 0; c < BLK_N / 32; ++c)
-        tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      tmem_wait_ld();
       const int k0 = kb * BLK_N;
       const bool masked = (k0 + BLK_N > L) || (P.causal && k0 + BLK_N - 1 > tq0);
       // allowed keys of this row in this block: k0 + c < lim
       const int lim = masked ? (P.causal ? min(L, q + 1) : L) - k0 : BLK_N;
-      if (masked) {
-#pragma unroll
-        for (int c = 0; c < BLK_N; ++c)
-          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
-      }
+      // Pass 1: the block's row max, two 64-column halves of S from TMEM.
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BLK_N; c += 4) {
-        mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-        mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(s_addr + 64 * hh, ra);
+        tmem_ld32(s_addr + 64 * hh + 32, rb);
+        tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (64 * hh + j >= lim) ra[j] = __float_as_uint(-INFINITY);
+            if (64 * hh + 32 + j >= lim) rb[j] = __float_as_uint(-INFINITY);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          mx0 = max3(mx0, __uint_as_float(ra[j]), __uint_as_float(ra[j + 1]));
+          mx1 = max3(mx1, __uint_as_float(rb[j]), __uint_as_float(rb[j + 1]));
+        }
       }
       const float mx = fmaxf(mx0, mx1);
       const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
@@ -345,36 +362,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float m_new = raise ? fmaxf(m_run, m_blk) : m_run;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m_run - m_use);  // e^{m - m'}: 1 when m is kept
-      float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
       const float2 negm = make_float2(-m_use, -m_use);
-      // P overwrites the first BLK_N/2 columns of S (two bf16 per column),
-      // written in two halves to keep fewer values live
+      float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
+      // Pass 2: p = 2^{c log2(e) s - m} in 32-column chunks, written as bf16
+      // over the first BLK_N/2 columns of S (chunk c of P lands on columns
+      // already read). The next chunk's load is in flight while this one is
+      // computed.
+      uint32_t cur[32], nxt[32];
+      tmem_ld32(s_addr, cur);
+      tmem_wait_ld();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[BLK_N / 4];
+      for (int c = 0; c < BLK_N; c += 32) {
+        if (c + 32 < BLK_N) tmem_ld32(s_addr + c + 32, nxt);
+        uint32_t pk[16];
 #pragma unroll
-        for (int cc = 0; cc < BLK_N / 2; cc += 4) {
-          const int c = h * (BLK_N / 2) + cc;
-          float2 x0 = __ffma2_rn(
-              make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cl2x2, negm);
+        for (int j = 0; j < 32; j += 4) {
+          float2 x0 = __ffma2_rn(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])),
+                                 cl2x2, negm);
           float2 x1 = __ffma2_rn(
-              make_float2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), cl2x2, negm);
+              make_float2(__uint_as_float(cur[j + 2]), __uint_as_float(cur[j + 3])), cl2x2, negm);
           x0.x = ex2_approx(x0.x);
           x0.y = ex2_approx(x0.y);
           x1.x = ex2_approx(x1.x);
           x1.y = ex2_approx(x1.y);
           if (masked) {  // forbidden keys get weight exactly 0 (also when c = 0)
-            if (c + 0 >= lim) x0.x = 0.f;
-            if (c + 1 >= lim) x0.y = 0.f;
-            if (c + 2 >= lim) x1.x = 0.f;
-            if (c + 3 >= lim) x1.y = 0.f;
+            if (c + j + 0 >= lim) x0.x = 0.f;
+            if (c + j + 1 >= lim) x0.y = 0.f;
+            if (c + j + 2 >= lim) x1.x = 0.f;
+            if (c + j + 3 >= lim) x1.y = 0.f;
           }
           sum = __fadd2_rn(sum, x0);
           sum_b = __fadd2_rn(sum_b, x1);
-          pk[cc / 2] = pack_bf16x2(x0.x, x0.y);
-          pk[cc / 2 + 1] = pack_bf16x2(x1.x, x1.y);
+          pk[j / 2] = pack_bf16x2(x0.x, x0.y);
+          pk[j / 2 + 1] = pack_bf16x2(x1.x, x1.y);
         }
-        tmem_st32(s_addr + 32 * h, pk);
+        tmem_st16(s_addr + c / 2, pk);
+        if (c + 32 < BLK_N) {
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
+        }
       }
       l_run = l_run * alpha + ((sum.x + sum.y) + (sum_b.x + sum_b.y));
       // merge: rescale this row of z by e^{m - m'} when m was raised; z must

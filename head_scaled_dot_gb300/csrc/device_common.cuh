@@ -69,6 +69,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not yet complete is suspended
+// in hardware for up to `hint_ns` (it wakes as soon as the phase completes),
+// so waiting warps do not spin on the scheduler that the issuing threads need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the barrier phase with the given parity has completed. Returns
 // false (and records MHA_ERR_DEVICE_TIMEOUT) after w.limit_ns, or at once when
 // another role of the CTA has already given up. Never spins without bound:
@@ -76,7 +92,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 static __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1; it != 0; ++it) {  // wraps after 2^32 polls at most
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
     if ((it & 31u) == 0) {
       if (*w.abort) return false;
       if (globaltimer_ns() - t0 > w.limit_ns) {
