@@ -150,6 +150,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* o_full = p_full + 2;            // [2] per tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  // blocks whose P has been consumed by tile 0's issuer (monotonic)
+  volatile int* tile0_progress = reinterpret_cast<volatile int*>(abort_flag + 1);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -165,6 +167,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&o_full[t], 1);
     }
     *abort_flag = 0;
+    *tile0_progress = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -265,9 +268,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         umma_commit(&o_full[t]);
         umma_commit(&v_empty[kb % C::STAGES]);  // this tile is done with V_kb
       };
+      // Tile 1 runs half a step behind tile 0: S_1 of block j is issued only
+      // once tile 0's softmax of block j is done, so the two tiles' softmaxes
+      // alternate (they share the exponential units and issue slots) and each
+      // overlaps the other tile's MMAs.
+      auto staggered = [&](int kb) -> bool {
+        return t == 0 || nb0 <= kb || counter_wait(tile0_progress, kb + 1, w);
+      };
       bool ok = nbt > 0 && mbar_wait(q_full, 0, w);
       int kb = 0;
-      if (ok && mbar_wait(&k_full[0], 0, w)) {
+      if (ok && mbar_wait(&k_full[0], 0, w) && staggered(0)) {
         tc_fence_after();
         issue_s(0);
         for (; kb < nbt; ++kb) {
@@ -277,10 +287,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
+          if (t == 0) *tile0_progress = kb + 1;
           tc_fence_after();
           issue_pv(kb);
           if (kb + 1 < nbt) {
-            if (!mbar_wait(&k_full[(kb + 1) % C::STAGES], ((kb + 1) / C::STAGES) & 1, w)) {
+            if (!mbar_wait(&k_full[(kb + 1) % C::STAGES], ((kb + 1) / C::STAGES) & 1, w) ||
+                !staggered(kb + 1)) {
               ok = false;
               break;
             }

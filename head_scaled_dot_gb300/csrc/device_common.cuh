@@ -92,7 +92,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 static __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1; it != 0; ++it) {  // wraps after 2^32 polls at most
-    if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*w.abort) return false;
       if (globaltimer_ns() - t0 > w.limit_ns) {
@@ -108,6 +108,25 @@ static __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t pa
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, w);
+}
+
+// Waits until the shared-memory counter reaches `target` (a monotonic count
+// written by another thread of the CTA). Bounded like mbar_wait.
+static __device__ __forceinline__ bool counter_wait(volatile int* ctr, int target, const WaitCtl& w) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1; it != 0; ++it) {
+    if (*ctr >= target) return true;
+    if ((it & 31u) == 0) {
+      if (*w.abort) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        report_error(w, MHA_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+  report_error(w, MHA_ERR_DEVICE_TIMEOUT);
+  return false;
 }
 
 // ---------------------------------------------------------------------------
