@@ -65,15 +65,18 @@ struct AttnTcParams {
   int valid_len[MHA_MAX_PADDED_BATCH];
 };
 
+// bytes after the K/V ring: barriers (up to 64 x 8 B) and the 2 KB exchange
+constexpr int EXTRA = 512 + 2 * 2 * 128 * 4;
+
 template <int DQK, int DV>
 struct ACfg {
   static constexpr int Q_TILE_BYTES = BLK_M * DQK * 2;
   static constexpr int K_BYTES = BLK_N * DQK * 2;
   static constexpr int V_BYTES = BLK_N * DV * 2;
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-  static constexpr int BUDGET = 227 * 1024 - 2 * Q_TILE_BYTES - 1024 - 512;
+  static constexpr int BUDGET = 227 * 1024 - 2 * Q_TILE_BYTES - 1024 - EXTRA;
   static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 4 ? 4 : (BUDGET / STAGE_BYTES);
-  static constexpr int SMEM = 2 * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + 512;
+  static constexpr int SMEM = 2 * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA;
   // TMEM columns: S of tile 0 and 1, then z (O) of tile 0 and 1.
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + DV;
@@ -150,8 +153,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* o_full = p_full + 2;            // [2] per tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  // blocks whose P has been consumed by tile 0's issuer (monotonic)
-  volatile int* tile0_progress = reinterpret_cast<volatile int*>(abort_flag + 1);
+  // partial row max / row sum exchange between partner softmax threads:
+  // [2 halves][2 slots][128 rows] floats
+  float* xchg = reinterpret_cast<float*>(bars + 64);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -163,11 +167,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 4);  // one arrival per softmax warp of the tile
+      mbar_init(&p_full[t], 8);  // one arrival per softmax warp
       mbar_init(&o_full[t], 1);
     }
     *abort_flag = 0;
-    *tile0_progress = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -268,16 +271,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         umma_commit(&o_full[t]);
         umma_commit(&v_empty[kb % C::STAGES]);  // this tile is done with V_kb
       };
-      // Tile 1 runs half a step behind tile 0: S_1 of block j is issued only
-      // once tile 0's softmax of block j is done, so the two tiles' softmaxes
-      // alternate (they share the exponential units and issue slots) and each
-      // overlaps the other tile's MMAs.
-      auto staggered = [&](int kb) -> bool {
-        return t == 0 || nb0 <= kb || counter_wait(tile0_progress, kb + 1, w);
-      };
       bool ok = nbt > 0 && mbar_wait(q_full, 0, w);
       int kb = 0;
-      if (ok && mbar_wait(&k_full[0], 0, w) && staggered(0)) {
+      if (ok && mbar_wait(&k_full[0], 0, w)) {
         tc_fence_after();
         issue_s(0);
         for (; kb < nbt; ++kb) {
@@ -287,12 +283,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
-          if (t == 0) *tile0_progress = kb + 1;
           tc_fence_after();
           issue_pv(kb);
           if (kb + 1 < nbt) {
-            if (!mbar_wait(&k_full[(kb + 1) % C::STAGES], ((kb + 1) / C::STAGES) & 1, w) ||
-                !staggered(kb + 1)) {
+            if (!mbar_wait(&k_full[(kb + 1) % C::STAGES], ((kb + 1) / C::STAGES) & 1, w)) {
               ok = false;
               break;
             }
@@ -323,144 +317,172 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   } else {
-    const int t = (warp - 4) / 4;  // tile of this warpgroup
-    const int g = warp & 3;        // TMEM lane slice 32*g .. 32*g+31
+    // Softmax: warps 4..11 take tile 0 then tile 1 for every key block, so
+    // the two tiles' softmaxes alternate (they share the exponential units)
+    // and each overlaps the other tile's MMAs. A row is split between the
+    // two warps that see the same TMEM lane slice (w and w + 4): `half`
+    // selects key columns [64 half, 64 half + 64) of S and value columns
+    // [half DV/2, (half + 1) DV/2) of z. The partners combine their partial
+    // row max through shared memory (a 64-thread named barrier) and keep
+    // partial row sums, added once at the end.
+    const int g = warp & 3;           // TMEM lane slice 32*g .. 32*g+31
+    const int half = (warp - 4) >> 2;  // 0: warps 4..7, 1: warps 8..11
     const int r = 32 * g + lane;
-    const int tq0 = q0 + t * BLK_M;
-    const int q = tq0 + r;
-    const int nblk = t ? nb1 : nb0;
     const uint32_t lane_off = static_cast<uint32_t>(32 * g) << 16;
-    const uint32_t s_addr = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
-    const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
     const float cl2 = P.cl2;
     const float2 cl2x2 = make_float2(cl2, cl2);
-    float m_run = -INFINITY, l_run = 0.f;
+    float* xch = xchg + 2 * 128 * half;        // this thread's slots: [2][128]
+    const float* pxch = xchg + 2 * 128 * (1 - half);  // the partner's
+    auto pair_sync = [&]() {
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + g) : "memory");
+    };
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    int xc = 0;  // exchanges so far (alternates the shared slots)
     bool ok = true;
-    for (int kb = 0; kb < nblk; ++kb) {
-      if (!mbar_wait(&s_full[t], kb & 1, w)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int k0 = kb * BLK_N;
-      const bool masked = (k0 + BLK_N > L) || (P.causal && k0 + BLK_N - 1 > tq0);
-      // allowed keys of this row in this block: k0 + c < lim
-      const int lim = masked ? (P.causal ? min(L, q + 1) : L) - k0 : BLK_N;
-      // Pass 1: the block's row max, two 64-column halves of S from TMEM.
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+    // Every (block, tile) step below runs exactly one pair barrier on both
+    // partners, whatever happened before (a partner that gave up on a wait
+    // still takes part), so the named barriers can never be left waiting.
+    for (int kb = 0; kb < nmax; ++kb) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(s_addr + 64 * hh, ra);
-        tmem_ld32(s_addr + 64 * hh + 32, rb);
+      for (int t = 0; t < 2; ++t) {
+        const int nblk = t ? nb1 : nb0;
+        if (kb >= nblk) continue;  // uniform across the pair
+        const int tq0 = q0 + t * BLK_M;
+        const int q = tq0 + r;
+        const uint32_t s_addr = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
+        const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
+        if (ok && !mbar_wait(&s_full[t], kb & 1, w)) ok = false;
+        if (!ok) {  // keep the pair in step, do no work
+          pair_sync();
+          ++xc;
+          continue;
+        }
+        tc_fence_after();
+        const int k0 = kb * BLK_N;
+        const bool masked = (k0 + BLK_N > L) || (P.causal && k0 + BLK_N - 1 > tq0);
+        // allowed keys of this row in this block: k0 + c < lim
+        const int lim = (masked ? (P.causal ? min(L, q + 1) : L) - k0 : BLK_N) - 64 * half;
+        uint32_t sr[64];
+        tmem_ld32(s_addr + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(s_addr + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_wait_ld();
         if (masked) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (64 * hh + j >= lim) ra[j] = __float_as_uint(-INFINITY);
-            if (64 * hh + 32 + j >= lim) rb[j] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < 64; ++c)
+            if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+          mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+        }
+        // combine with the partner's half of the row; after this barrier both
+        // halves of S are in registers, so P may overwrite its columns
+        xch[128 * (xc & 1) + r] = fmaxf(mx0, mx1);
+        pair_sync();
+        const float mx = fmaxf(xch[128 * (xc & 1) + r], pxch[128 * (xc & 1) + r]);
+        ++xc;
+        const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
+        // raise the running max only past the threshold (or on the first block)
+        const bool raise =
+            (m_run[t] == -INFINITY) ? true : (m_blk > m_run[t] + RESCALE_LOG2);
+        const float m_new = raise ? fmaxf(m_run[t], m_blk) : m_run[t];
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2_approx(m_run[t] - m_use);  // e^{m - m'}: 1 when m is kept
+        const float2 negm = make_float2(-m_use, -m_use);
+        float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
+        // p = 2^{c log2(e) s - m} as bf16 into this half's P columns
+        // [32 half, 32 half + 32) of S (two bf16 per column)
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float2 x0 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[c + j]), __uint_as_float(sr[c + j + 1])), cl2x2,
+                negm);
+            float2 x1 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[c + j + 2]), __uint_as_float(sr[c + j + 3])),
+                cl2x2, negm);
+            x0.x = ex2_approx(x0.x);
+            x0.y = ex2_approx(x0.y);
+            x1.x = ex2_approx(x1.x);
+            x1.y = ex2_approx(x1.y);
+            if (masked) {  // forbidden keys get weight exactly 0 (also when c = 0)
+              if (c + j + 0 >= lim) x0.x = 0.f;
+              if (c + j + 1 >= lim) x0.y = 0.f;
+              if (c + j + 2 >= lim) x1.x = 0.f;
+              if (c + j + 3 >= lim) x1.y = 0.f;
+            }
+            sum = __fadd2_rn(sum, x0);
+            sum_b = __fadd2_rn(sum_b, x1);
+            pk[j / 2] = pack_bf16x2(x0.x, x0.y);
+            pk[j / 2 + 1] = pack_bf16x2(x1.x, x1.y);
+          }
+          tmem_st16(s_addr + 32 * half + c / 2, pk);
+        }
+        l_run[t] = l_run[t] * alpha + ((sum.x + sum.y) + (sum_b.x + sum_b.y));
+        // merge: rescale this row of z by e^{m - m'} when m was raised; z must
+        // already hold every earlier block (wait for the previous z += P V)
+        if (__any_sync(0xffffffffu, kb > 0 && raise)) {
+          if (!mbar_wait(&o_full[t], (kb - 1) & 1, w)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c) {
+            uint32_t o[32];
+            const uint32_t oa = o_addr + half * (DV / 2) + 32 * c;
+            tmem_ld32(oa, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float2 v = __fmul2_rn(
+                  make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
+                  make_float2(alpha, alpha));
+              o[j] = __float_as_uint(v.x);
+              o[j + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(oa, o);
           }
         }
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          mx0 = max3(mx0, __uint_as_float(ra[j]), __uint_as_float(ra[j + 1]));
-          mx1 = max3(mx1, __uint_as_float(rb[j]), __uint_as_float(rb[j + 1]));
-        }
+        m_run[t] = m_new;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
       }
-      const float mx = fmaxf(mx0, mx1);
-      const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
-      // raise the running max only past the threshold (or on the first block)
-      const bool raise = (m_run == -INFINITY) ? true : (m_blk > m_run + RESCALE_LOG2);
-      const float m_new = raise ? fmaxf(m_run, m_blk) : m_run;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run - m_use);  // e^{m - m'}: 1 when m is kept
-      const float2 negm = make_float2(-m_use, -m_use);
-      float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
-      // Pass 2: p = 2^{c log2(e) s - m} in 32-column chunks, written as bf16
-      // over the first BLK_N/2 columns of S (chunk c of P lands on columns
-      // already read). The next chunk's load is in flight while this one is
-      // computed.
-      uint32_t cur[32], nxt[32];
-      tmem_ld32(s_addr, cur);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < BLK_N; c += 32) {
-        if (c + 32 < BLK_N) tmem_ld32(s_addr + c + 32, nxt);
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float2 x0 = __ffma2_rn(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])),
-                                 cl2x2, negm);
-          float2 x1 = __ffma2_rn(
-              make_float2(__uint_as_float(cur[j + 2]), __uint_as_float(cur[j + 3])), cl2x2, negm);
-          x0.x = ex2_approx(x0.x);
-          x0.y = ex2_approx(x0.y);
-          x1.x = ex2_approx(x1.x);
-          x1.y = ex2_approx(x1.y);
-          if (masked) {  // forbidden keys get weight exactly 0 (also when c = 0)
-            if (c + j + 0 >= lim) x0.x = 0.f;
-            if (c + j + 1 >= lim) x0.y = 0.f;
-            if (c + j + 2 >= lim) x1.x = 0.f;
-            if (c + j + 3 >= lim) x1.y = 0.f;
-          }
-          sum = __fadd2_rn(sum, x0);
-          sum_b = __fadd2_rn(sum_b, x1);
-          pk[j / 2] = pack_bf16x2(x0.x, x0.y);
-          pk[j / 2 + 1] = pack_bf16x2(x1.x, x1.y);
-        }
-        tmem_st16(s_addr + c / 2, pk);
-        if (c + 32 < BLK_N) {
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
-        }
-      }
-      l_run = l_run * alpha + ((sum.x + sum.y) + (sum_b.x + sum_b.y));
-      // merge: rescale this row of z by e^{m - m'} when m was raised; z must
-      // already hold every earlier block (wait for the previous z += P V)
-      if (__any_sync(0xffffffffu, kb > 0 && raise)) {
-        if (!mbar_wait(&o_full[t], (kb - 1) & 1, w)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + 32 * c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float2 v = __fmul2_rn(
-                make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
-                make_float2(alpha, alpha));
-            o[j] = __float_as_uint(v.x);
-            o[j + 1] = __float_as_uint(v.y);
-          }
-          tmem_st32(o_addr + 32 * c, o);
-        }
-      }
-      m_run = m_new;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    if (nblk == 0) {
-      // the whole tile is padding (tile 1 only): its rows are zero
-      if (q < P.n_q) {
-        uint4* dst = reinterpret_cast<uint4*>(Zg + zbase + (long long)q * zrow_stride);
+    // Epilogue: z / l for this half of each row, in the concatenated layout.
 #pragma unroll
-        for (int j = 0; j < DV / 8; ++j) dst[j] = make_uint4(0, 0, 0, 0);
+    for (int t = 0; t < 2; ++t) {
+      const int nblk = t ? nb1 : nb0;
+      const int q = q0 + t * BLK_M + r;
+      const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
+      __nv_bfloat16* zrow = Zg + zbase + (long long)q * zrow_stride + half * (DV / 2);
+      if (nblk == 0) {
+        // the whole tile is padding (tile 1 only): its rows are zero
+        if (q < P.n_q) {
+#pragma unroll
+          for (int j = 0; j < DV / 16; ++j) reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
       }
-    } else if (ok && mbar_wait(&o_full[t], (nblk - 1) & 1, w)) {
+      // the row sum is the two partners' partial sums (same running max)
+      xch[128 * (xc & 1) + r] = l_run[t];
+      pair_sync();
+      const float l_tot = l_run[t] + pxch[128 * (xc & 1) + r];
+      ++xc;
+      if (!ok || !mbar_wait(&o_full[t], (nblk - 1) & 1, w)) continue;
       tc_fence_after();
       const bool computed = q < q_end;
-      const float inv = computed ? 1.f / l_run : 0.f;
+      const float inv = computed ? 1.f / l_tot : 0.f;
 #pragma unroll
-      for (int c = 0; c < DV / 32; ++c) {
+      for (int c = 0; c < DV / 64; ++c) {
         uint32_t o[32];
-        tmem_ld32(o_addr + 32 * c, o);
+        tmem_ld32(o_addr + half * (DV / 2) + 32 * c, o);
         tmem_wait_ld();
         if (q < P.n_q) {
           uint32_t pk[16];
@@ -469,7 +491,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             pk[j] = computed ? pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
                                            __uint_as_float(o[2 * j + 1]) * inv)
                              : 0u;
-          uint4* dst = reinterpret_cast<uint4*>(Zg + zbase + (long long)q * zrow_stride + 32 * c);
+          uint4* dst = reinterpret_cast<uint4*>(zrow + 32 * c);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
