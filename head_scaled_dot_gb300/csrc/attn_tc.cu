@@ -98,6 +98,20 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+// Maximum of 64 values as a tree of three-input maxima (depth 4).
+__device__ __forceinline__ float max64(const uint32_t (&v)[64]) {
+  float a[22], b[8];
+#pragma unroll
+  for (int i = 0; i < 21; ++i)
+    a[i] = max3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]),
+                __uint_as_float(v[3 * i + 2]));
+  a[21] = __uint_as_float(v[63]);
+#pragma unroll
+  for (int i = 0; i < 7; ++i) b[i] = max3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[7] = a[21];
+  return max3(max3(b[0], b[1], b[2]), max3(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
+}
+
 // Number of 128-key blocks a tile starting at row tq0 must fold (0 when all
 // its rows are padding).
 __device__ __forceinline__ int tile_blocks(const AttnTcParams& P, int tq0, int L, int q_end) {
@@ -367,19 +381,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld32(s_addr + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_wait_ld();
         if (masked) {
+          // forbidden keys get s = -inf, hence weight 2^{-inf} = 0 exactly
+          // (the scale cl2 is positive, never 0); blocks without forbidden
+          // keys skip this branch
 #pragma unroll
           for (int c = 0; c < 64; ++c)
             if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
         }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-          mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-        }
         // combine with the partner's half of the row; after this barrier both
         // halves of S are in registers, so P may overwrite its columns
-        xch[128 * (xc & 1) + r] = fmaxf(mx0, mx1);
+        xch[128 * (xc & 1) + r] = max64(sr);
         pair_sync();
         const float mx = fmaxf(xch[128 * (xc & 1) + r], pxch[128 * (xc & 1) + r]);
         ++xc;
@@ -409,12 +420,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             x0.y = ex2_approx(x0.y);
             x1.x = ex2_approx(x1.x);
             x1.y = ex2_approx(x1.y);
-            if (masked) {  // forbidden keys get weight exactly 0 (also when c = 0)
-              if (c + j + 0 >= lim) x0.x = 0.f;
-              if (c + j + 1 >= lim) x0.y = 0.f;
-              if (c + j + 2 >= lim) x1.x = 0.f;
-              if (c + j + 3 >= lim) x1.y = 0.f;
-            }
             sum = __fadd2_rn(sum, x0);
             sum_b = __fadd2_rn(sum_b, x1);
             pk[j / 2] = pack_bf16x2(x0.x, x0.y);
@@ -546,7 +551,11 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
   P.n_q = a.n_q;
   P.n_k = a.n_k;
   P.h = a.h;
-  P.cl2 = fabsf(a.c) * 1.4426950408889634f;
+  // |c| log2(e), kept at 1e-30 or above so that a masked score (-inf) stays
+  // -inf after scaling; for c = 0 (or |c| below that) every allowed score
+  // scales to within 1e-26 of 0 and gets weight 2^0 = 1: the uniform
+  // distribution over the allowed keys, as softmax of all-zero scores
+  P.cl2 = fmaxf(fabsf(a.c) * 1.4426950408889634f, 1e-30f);
   P.negate = a.c < 0.f;
   P.causal = a.causal;
   P.padding = a.padding;
