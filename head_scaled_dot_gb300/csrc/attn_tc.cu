@@ -504,10 +504,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   }
+  // Every lane of a warp meets here before the CTA-wide barrier: a barrier
+  // counts whole warps, so a warp must not reach it split across branches.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }

@@ -85,6 +85,46 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// As mbar_try_wait, without acquire ordering. For the thread that issues
+// tcgen05.mma: there an acquire wait costs the tensor pipe a couple of hundred
+// cycles (it orders behind the thread's MMAs still in flight), a relaxed one
+// nothing.
+__device__ __forceinline__ bool mbar_try_wait_relaxed(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait with mbar_try_wait_relaxed (see there), for the MMA-issuing
+// thread. What it waits for is complete when the phase completes: TMA data
+// (complete_tx) or tensor-memory writes that the writers finished
+// (tcgen05.wait::st, tcgen05.fence::before_thread_sync) before arriving; the
+// caller issues its MMAs only after the wait returns, behind
+// tcgen05.fence::after_thread_sync.
+static __device__ __forceinline__ bool mbar_wait_relaxed(uint64_t* bar, uint32_t parity,
+                                                         const WaitCtl& w) {
+  if (mbar_try_wait_relaxed(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1; it != 0; ++it) {
+    if (mbar_try_wait_relaxed(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*w.abort) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        report_error(w, MHA_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  report_error(w, MHA_ERR_DEVICE_TIMEOUT);
+  return false;
+}
+
 // Waits until the barrier phase with the given parity has completed. Returns
 // false (and records MHA_ERR_DEVICE_TIMEOUT) after w.limit_ns, or at once when
 // another role of the CTA has already given up. Never spins without bound:
@@ -92,7 +132,9 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 static __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1; it != 0; ++it) {  // wraps after 2^32 polls at most
-    if (mbar_try_wait(bar, parity)) return true;
+    // suspended in hardware until the phase completes (or 20 us pass), so
+    // that waiting threads do not poll the barrier the others need
+    if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
     if ((it & 31u) == 0) {
       if (*w.abort) return false;
       if (globaltimer_ns() - t0 > w.limit_ns) {
@@ -266,6 +308,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -291,6 +343,31 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// As tmem_wait_ld, and ties the wait to the registers of one 16-column load
+// still in flight, so that no use of them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_ld_r(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
+// As tmem_wait_ld, and ties the wait to the registers of one 32-column load
+// still in flight, so that no use of them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_ld_r(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() {

@@ -232,23 +232,15 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
   }
+  // Every lane of a warp meets here before the CTA-wide barrier: a barrier
+  // counts whole warps, so a warp must not reach it split across branches.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-}
-
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
 }
 
 template <int BN>

@@ -57,6 +57,7 @@ struct AttnArgs {
 // Kernel limit for bounded waits (nanoseconds).
 uint64_t wait_limit_ns();
 void count_launch(int n = 1);
+int num_sms();
 
 // CUDA-core kernels (fp32; the bf16 instantiation is kept for tests).
 mha_status gemm_simt(const GemmProblem* probs, int nprob, mha_dtype dt, cudaStream_t s);

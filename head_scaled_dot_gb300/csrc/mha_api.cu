@@ -21,6 +21,15 @@ void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_r
 // (a whole kernel takes milliseconds), short enough to free a shared GPU fast.
 uint64_t wait_limit_ns() { return 2000000000ull; }
 
+// Streaming multiprocessors of the current device (persistent grids).
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
 // ---------------------------------------------------------------------------
 // TMA descriptors
 // ---------------------------------------------------------------------------
