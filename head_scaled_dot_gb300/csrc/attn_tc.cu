@@ -63,6 +63,7 @@ struct AttnTcParams {
   int32_t* err;
   uint64_t limit_ns;
   int valid_len[MHA_MAX_PADDED_BATCH];
+  float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale (1: no gate)
 };
 
 // bytes after the K/V ring: barriers (up to 64 x 8 B) and the 2 KB exchange
@@ -483,7 +484,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok || !mbar_wait(&o_full[t], (nblk - 1) & 1, w)) continue;
       tc_fence_after();
       const bool computed = q < q_end;
-      const float inv = computed ? 1.f / l_tot : 0.f;
+      const float inv = computed ? P.head_gate[head] / l_tot : 0.f;
 #pragma unroll
       for (int c = 0; c < DV / 64; ++c) {
         uint32_t o[32];
@@ -566,6 +567,8 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
   P.limit_ns = wait_limit_ns();
   for (int b = 0; b < MHA_MAX_PADDED_BATCH; ++b)
     P.valid_len[b] = (a.padding && b < a.B) ? a.valid_len_host[b] : a.n_k;
+  for (int i = 0; i < MHA_MAX_GATED_HEADS; ++i)
+    P.head_gate[i] = (a.head_gate_host && i < a.h) ? a.head_gate_host[i] : 1.f;
   if (a.d_h == 64 && a.d_vh == 64) return launch<64, 64>(P, a.B, a.h, a.n_q, s);
   if (a.d_h == 128 && a.d_vh == 128) return launch<128, 128>(P, a.B, a.h, a.n_q, s);
   if (a.d_h == 64 && a.d_vh == 128) return launch<64, 128>(P, a.B, a.h, a.n_q, s);

@@ -292,7 +292,11 @@ mha_status gemm_tc(const GemmProblem* probs, int nprob, int32_t* err, cudaStream
     if (!make_tmap_bf16(&P.amap[i], pr.A, 2, adims, astr, abox, true) ||
         !make_tmap_bf16(&P.bmap[i], pr.W, 2, bdims, bstr, bbox, true))
       return MHA_ERR_CUDA;
-    if (pr.cols_per_group % 32 && pr.cols_per_group != pr.N) return MHA_ERR_UNSUPPORTED;
+    // 16-byte vector stores in the epilogue: every row pitch, group stride and
+    // 32-column chunk offset is a multiple of 8 elements
+    if (pr.cols_per_group % 8 || pr.N % 8 || pr.s_row % 8 || pr.s_group_col % 8 ||
+        pr.s_group_row % 8)
+      return MHA_ERR_UNSUPPORTED;
   }
   return all256 ? launch<256>(P, s) : launch<128>(P, s);
 }

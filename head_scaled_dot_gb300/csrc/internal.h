@@ -51,6 +51,7 @@ struct AttnArgs {
   int padding;          // keys j < valid_len[b]
   int pad_queries;      // rows i >= valid_len[b] are not computed (Z row = 0)
   const int32_t* valid_len_host;  // B entries when padding
+  const float* head_gate_host;    // h entries, or null (all 1): head i's output is scaled by it
   int32_t* err;
 };
 

@@ -134,14 +134,18 @@ Layout layout(int B, int n_q, int n_k, int h, int d_h, int d_vh, mha_dtype dt) {
   return L;
 }
 
-// Shape support of each compute path (MHA_OK or MHA_ERR_UNSUPPORTED).
+// Head sizes every path handles: 1 .. MAX_HEAD_DIM. bf16 heads of 64 or 128
+// run on the tensor cores, other sizes on the CUDA-core kernel.
+constexpr int MAX_HEAD_DIM = 256;
+
 mha_status check_head_dims(int d_h, int d_vh, mha_dtype dt) {
-  if (dt == MHA_DTYPE_BF16) {
-    if ((d_h != 64 && d_h != 128) || (d_vh != 64 && d_vh != 128)) return MHA_ERR_UNSUPPORTED;
-  } else {
-    if (d_h > 128 || d_vh > 128) return MHA_ERR_UNSUPPORTED;
-  }
+  (void)dt;
+  if (d_h > MAX_HEAD_DIM || d_vh > MAX_HEAD_DIM) return MHA_ERR_UNSUPPORTED;
   return MHA_OK;
+}
+
+bool tc_head_dims(int d_h, int d_vh) {
+  return (d_h == 64 || d_h == 128) && (d_vh == 64 || d_vh == 128);
 }
 
 // Elements beyond 2^31 per tensor are not addressed by every index path.
@@ -159,22 +163,29 @@ mha_status check_valid_len(mha_mask_kind mask, const int32_t* valid_len, int B, 
   return MHA_OK;
 }
 
-mha_status run_qkv(const void* X_q, const void* X_kv, const void* W_Q, const void* W_K,
-                   const void* W_V, void* Q, void* K, void* V, int B, int n_q, int n_k,
-                   int d_model, int h, int d_h, int d_vh, mha_dtype dt, int32_t* err,
-                   cudaStream_t s) {
-  const void* Xk = X_kv ? X_kv : X_q;
+// The three projections as one grouped GEMM: X_q (d_q wide) W_Q, X_k (d_k
+// wide) W_K, X_v (d_v wide) W_V, each written head-split.
+mha_status run_qkv(const void* X_q, const void* X_k, const void* X_v, const void* W_Q,
+                   const void* W_K, const void* W_V, void* Q, void* K, void* V, int B, int n_q,
+                   int n_k, int d_q, int d_k, int d_v, int h, int d_h, int d_vh, mha_dtype dt,
+                   int32_t* err, cudaStream_t s) {
   GemmProblem p[3] = {
-      head_split_problem(X_q, W_Q, Q, B, n_q, h, d_h, d_model),
-      head_split_problem(Xk, W_K, K, B, n_k, h, d_h, d_model),
-      head_split_problem(Xk, W_V, V, B, n_k, h, d_vh, d_model),
+      head_split_problem(X_q, W_Q, Q, B, n_q, h, d_h, d_q),
+      head_split_problem(X_k, W_K, K, B, n_k, h, d_h, d_k),
+      head_split_problem(X_v, W_V, V, B, n_k, h, d_vh, d_v),
   };
   if (dt == MHA_DTYPE_BF16) return gemm_tc(p, 3, err, s);
   return gemm_simt(p, 3, dt, s);
 }
 
+// bf16 alignment the tensor-memory-access (TMA) GEMM needs: 16-byte row
+// pitches and base addresses.
+bool bf16_gemm_ok(int d_in, int width, const void* X, const void* W) {
+  return d_in % 8 == 0 && width % 8 == 0 && aligned16(X) && aligned16(W);
+}
+
 mha_status run_attention(const AttnArgs& a, mha_dtype dt, cudaStream_t s) {
-  if (dt == MHA_DTYPE_BF16) return attention_tc(a, s);
+  if (dt == MHA_DTYPE_BF16 && tc_head_dims(a.d_h, a.d_vh)) return attention_tc(a, s);
   return attention_simt(a, dt, s);
 }
 
@@ -183,6 +194,49 @@ mha_status run_out(const void* Z, const void* W_O, void* Y, int B, int n_q, int 
   GemmProblem p = plain_problem(Z, W_O, Y, B * n_q, d_o, h * d_vh);
   if (dt == MHA_DTYPE_BF16) return gemm_tc(&p, 1, err, s);
   return gemm_simt(&p, 1, dt, s);
+}
+
+// The attention step with its checks; head_gate (host, h floats) may be null.
+mha_status attention_step(const void* Q, const void* K, const void* V, void* Z, int B, int n_q,
+                          int n_k, int h, int d_h, int d_vh, float c, mha_mask_kind mask,
+                          const int32_t* valid_len, int self_attention,
+                          const float* head_gate, mha_dtype dt, int32_t* dev_error,
+                          void* stream) {
+  if (!Q || !K || !V || !Z) return MHA_ERR_INVALID_ARG;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
+    return MHA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt) || !mask_ok(mask) || !isfinite(c)) return MHA_ERR_INVALID_ARG;
+  if (has_causal(mask) && n_q != n_k) return MHA_ERR_INVALID_ARG;
+  if (self_attention && n_q != n_k) return MHA_ERR_INVALID_ARG;
+  mha_status st = check_valid_len(mask, valid_len, B, n_k);
+  if (st != MHA_OK) return st;
+  st = check_head_dims(d_h, d_vh, dt);
+  if (st != MHA_OK) return st;
+  if (!fits((long long)B * h, n_q, d_h) || !fits((long long)B * h, n_k, d_h) ||
+      !fits((long long)B * h, n_k, d_vh) || !fits((long long)B * h, n_q, d_vh))
+    return MHA_ERR_UNSUPPORTED;
+  if (dt == MHA_DTYPE_BF16 && tc_head_dims(d_h, d_vh) &&
+      (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Z)))
+    return MHA_ERR_UNSUPPORTED;
+  AttnArgs a{};
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.Z = Z;
+  a.B = B;
+  a.n_q = n_q;
+  a.n_k = n_k;
+  a.h = h;
+  a.d_h = d_h;
+  a.d_vh = d_vh;
+  a.c = c;
+  a.causal = has_causal(mask);
+  a.padding = has_padding(mask);
+  a.pad_queries = has_padding(mask) && self_attention;
+  a.valid_len_host = valid_len;
+  a.head_gate_host = head_gate;
+  a.err = dev_error;
+  return run_attention(a, dt, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -226,53 +280,23 @@ mha_status mha_qkv_projection(const void* X_q, const void* X_kv, const void* W_Q
   if (!fits(B, n_q, d_model) || !fits(B, n_k, d_model) || !fits(B, n_q, h * d_h) ||
       !fits(B, n_k, h * (long long)d_vh))
     return MHA_ERR_UNSUPPORTED;
+  const void* Xk = X_kv ? X_kv : X_q;
   if (dt == MHA_DTYPE_BF16) {
-    if (d_model % 8 || !aligned16(X_q) || (X_kv && !aligned16(X_kv)) || !aligned16(W_Q) ||
-        !aligned16(W_K) || !aligned16(W_V) || !aligned16(Q) || !aligned16(K) || !aligned16(V))
+    if (d_h % 8 || d_vh % 8 || !bf16_gemm_ok(d_model, h * d_h, X_q, W_Q) || !bf16_gemm_ok(d_model, h * d_h, Xk, W_K) ||
+        !bf16_gemm_ok(d_model, h * d_vh, Xk, W_V) || !aligned16(Q) || !aligned16(K) ||
+        !aligned16(V))
       return MHA_ERR_UNSUPPORTED;
   }
-  return run_qkv(X_q, X_kv, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_model, h, d_h, d_vh, dt,
-                 dev_error, static_cast<cudaStream_t>(stream));
+  return run_qkv(X_q, Xk, Xk, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_model, d_model, d_model, h,
+                 d_h, d_vh, dt, dev_error, static_cast<cudaStream_t>(stream));
 }
 
 mha_status mha_attention(const void* Q, const void* K, const void* V, void* Z, int B, int n_q,
                          int n_k, int h, int d_h, int d_vh, float c, mha_mask_kind mask,
                          const int32_t* valid_len, int self_attention, mha_dtype dt,
                          int32_t* dev_error, void* stream) {
-  if (!Q || !K || !V || !Z) return MHA_ERR_INVALID_ARG;
-  if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
-    return MHA_ERR_INVALID_ARG;
-  if (!dtype_ok(dt) || !mask_ok(mask) || !isfinite(c)) return MHA_ERR_INVALID_ARG;
-  if (has_causal(mask) && n_q != n_k) return MHA_ERR_INVALID_ARG;
-  if (self_attention && n_q != n_k) return MHA_ERR_INVALID_ARG;
-  mha_status st = check_valid_len(mask, valid_len, B, n_k);
-  if (st != MHA_OK) return st;
-  st = check_head_dims(d_h, d_vh, dt);
-  if (st != MHA_OK) return st;
-  if (!fits((long long)B * h, n_q, d_h) || !fits((long long)B * h, n_k, d_h) ||
-      !fits((long long)B * h, n_k, d_vh) || !fits((long long)B * h, n_q, d_vh))
-    return MHA_ERR_UNSUPPORTED;
-  if (dt == MHA_DTYPE_BF16 &&
-      (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Z)))
-    return MHA_ERR_UNSUPPORTED;
-  AttnArgs a{};
-  a.Q = Q;
-  a.K = K;
-  a.V = V;
-  a.Z = Z;
-  a.B = B;
-  a.n_q = n_q;
-  a.n_k = n_k;
-  a.h = h;
-  a.d_h = d_h;
-  a.d_vh = d_vh;
-  a.c = c;
-  a.causal = has_causal(mask);
-  a.padding = has_padding(mask);
-  a.pad_queries = has_padding(mask) && self_attention;
-  a.valid_len_host = valid_len;
-  a.err = dev_error;
-  return run_attention(a, dt, static_cast<cudaStream_t>(stream));
+  return attention_step(Q, K, V, Z, B, n_q, n_k, h, d_h, d_vh, c, mask, valid_len,
+                        self_attention, nullptr, dt, dev_error, stream);
 }
 
 mha_status mha_output_projection(const void* Z, const void* W_O, void* Y, int B, int n_q, int h,
@@ -289,31 +313,41 @@ mha_status mha_output_projection(const void* Z, const void* W_O, void* Y, int B,
                  static_cast<cudaStream_t>(stream));
 }
 
-mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q, const void* W_K,
-                       const void* W_V, const void* W_O, void* Y, int B, int n_q, int n_k,
-                       int d_model, int h, int d_h, int d_vh, int d_o, float c,
-                       mha_mask_kind mask, const int32_t* valid_len, mha_dtype dt,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+mha_status mha_forward_general(const void* X_q, const void* X_k, const void* X_v,
+                               const void* W_Q, const void* W_K, const void* W_V,
+                               const void* W_O, void* Y, int B, int n_q, int n_k, int d_q,
+                               int d_k, int d_v, int h, int d_h, int d_vh, int d_o, float c,
+                               mha_mask_kind mask, const int32_t* valid_len, int self_attention,
+                               const float* head_gate, mha_dtype dt, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   // Host-side checks, all before anything is enqueued.
-  if (!X_q || !W_Q || !W_K || !W_V || !W_O || !Y) return MHA_ERR_INVALID_ARG;
-  if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0 ||
-      d_o <= 0)
+  if (!X_q || !X_k || !X_v || !W_Q || !W_K || !W_V || !W_O || !Y) return MHA_ERR_INVALID_ARG;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || d_q <= 0 || d_k <= 0 || d_v <= 0 || h <= 0 ||
+      d_h <= 0 || d_vh <= 0 || d_o <= 0)
     return MHA_ERR_INVALID_ARG;
   if (!dtype_ok(dt) || !mask_ok(mask) || !isfinite(c)) return MHA_ERR_INVALID_ARG;
-  const bool self_attn = X_kv == nullptr;
-  if (self_attn && n_k != n_q) return MHA_ERR_INVALID_ARG;
+  if (self_attention && n_k != n_q) return MHA_ERR_INVALID_ARG;
   if (has_causal(mask) && n_q != n_k) return MHA_ERR_INVALID_ARG;
   mha_status st = check_valid_len(mask, valid_len, B, n_k);
   if (st != MHA_OK) return st;
   st = check_head_dims(d_h, d_vh, dt);
   if (st != MHA_OK) return st;
-  if (dt == MHA_DTYPE_BF16 && (d_model % 8 || d_o % 8)) return MHA_ERR_UNSUPPORTED;
+  if (head_gate) {
+    if (h > MHA_MAX_GATED_HEADS) return MHA_ERR_UNSUPPORTED;
+    for (int i = 0; i < h; ++i)
+      if (!isfinite(head_gate[i])) return MHA_ERR_INVALID_ARG;
+  }
+  if (!fits(B, n_q, d_q) || !fits(B, n_k, d_k) || !fits(B, n_k, d_v) ||
+      !fits(B, n_q, (long long)h * d_h) || !fits(B, n_k, (long long)h * d_h) ||
+      !fits(B, n_k, (long long)h * d_vh) || !fits(B, n_q, d_o))
+    return MHA_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MHA_ERR_WORKSPACE;
   const Layout L = layout(B, n_q, n_k, h, d_h, d_vh, dt);
   if (workspace_bytes < L.total) return MHA_ERR_WORKSPACE;
-  if (dt == MHA_DTYPE_BF16 && (!aligned16(X_q) || (X_kv && !aligned16(X_kv)) ||
-                               !aligned16(W_Q) || !aligned16(W_K) || !aligned16(W_V) ||
-                               !aligned16(W_O) || !aligned16(Y)))
+  if (dt == MHA_DTYPE_BF16 &&
+      (d_h % 8 || d_vh % 8 || !bf16_gemm_ok(d_q, h * d_h, X_q, W_Q) ||
+       !bf16_gemm_ok(d_k, h * d_h, X_k, W_K) ||
+       !bf16_gemm_ok(d_v, h * d_vh, X_v, W_V) || !bf16_gemm_ok(h * d_vh, d_o, W_O, Y)))
     return MHA_ERR_UNSUPPORTED;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -324,13 +358,28 @@ mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q, const
   void* V = ws + L.v;
   void* Z = ws + L.z;
   if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return MHA_ERR_CUDA;
-  st = mha_qkv_projection(X_q, X_kv, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_model, h, d_h,
-                          d_vh, dt, err, stream);
+  st = run_qkv(X_q, X_k, X_v, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_q, d_k, d_v, h, d_h, d_vh,
+               dt, err, s);
   if (st != MHA_OK) return st;
-  st = mha_attention(Q, K, V, Z, B, n_q, n_k, h, d_h, d_vh, c, mask, valid_len,
-                     self_attn ? 1 : 0, dt, err, stream);
+  st = attention_step(Q, K, V, Z, B, n_q, n_k, h, d_h, d_vh, c, mask, valid_len,
+                      self_attention ? 1 : 0, head_gate, dt, err, stream);
   if (st != MHA_OK) return st;
   return mha_output_projection(Z, W_O, Y, B, n_q, h, d_vh, d_o, dt, err, stream);
+}
+
+mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q, const void* W_K,
+                       const void* W_V, const void* W_O, void* Y, int B, int n_q, int n_k,
+                       int d_model, int h, int d_h, int d_vh, int d_o, float c,
+                       mha_mask_kind mask, const int32_t* valid_len, mha_dtype dt,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!X_q) return MHA_ERR_INVALID_ARG;
+  const bool self_attn = X_kv == nullptr;
+  if (self_attn && n_k != n_q) return MHA_ERR_INVALID_ARG;
+  const void* Xkv = self_attn ? X_q : X_kv;
+  return mha_forward_general(X_q, Xkv, Xkv, W_Q, W_K, W_V, W_O, Y, B, n_q, n_k, d_model,
+                             d_model, d_model, h, d_h, d_vh, d_o, c, mask, valid_len,
+                             self_attn ? 1 : 0, nullptr, dt, workspace, workspace_bytes,
+                             stream);
 }
 
 mha_status mha_get_device_error(void* error_word, void* stream) {

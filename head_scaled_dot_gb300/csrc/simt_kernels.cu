@@ -102,7 +102,6 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
 
 constexpr int AT_ROWS = 32;  // query rows per CTA (4 per warp)
 constexpr int AT_KEYS = 32;  // keys per block (one per lane)
-constexpr int AT_DMAX = 128;
 
 struct AttnParams {
   const void* Q;
@@ -113,6 +112,7 @@ struct AttnParams {
   float c;
   int causal, padding, pad_queries;
   int valid_len[MHA_MAX_PADDED_BATCH];
+  float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale (1: no gate)
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -129,8 +129,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // grid (ceil(n_q / 32), h, B), 256 threads. Lane j of a warp scores key j of
 // the current 32-key block for one query row; the block's summary
-// (m_blk, l_blk, z_blk) is merged into the row's running summary.
-template <typename T>
+// (m_blk, l_blk, z_blk) is merged into the row's running summary. Head sizes
+// up to AT_DMAX (d_vh columns: lane + 32 t).
+template <typename T, int AT_DMAX>
 __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_constant__ AttnParams P) {
   extern __shared__ float sm[];
   const int dq = P.d_h, dv = P.d_vh;
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_consta
     const int q = q0 + warp * 4 + i;
     if (q >= P.n_q) continue;
     const bool computed = q < q_end;
-    const float inv = computed ? 1.f / l_run[i] : 0.f;
+    const float inv = computed ? P.head_gate[head] / l_run[i] : 0.f;
     T* zrow = Zg + ((long long)b * P.n_q + q) * (long long)P.h * dv + (long long)head * dv;
 #pragma unroll
     for (int t = 0; t < AT_DMAX / 32; ++t) {
@@ -243,8 +244,23 @@ mha_status gemm_simt(const GemmProblem* probs, int nprob, mha_dtype dt, cudaStre
   return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
+namespace {
+
+template <typename T, int DMAX>
+mha_status launch_attention_simt(const AttnParams& P, const dim3& grid, size_t smem,
+                                 cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(attention_simt_kernel<T, DMAX>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return MHA_ERR_CUDA;
+  attention_simt_kernel<T, DMAX><<<grid, 256, smem, s>>>(P);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+}  // namespace
+
 mha_status attention_simt(const AttnArgs& a, mha_dtype dt, cudaStream_t s) {
-  if (a.d_h > AT_DMAX || a.d_vh > AT_DMAX) return MHA_ERR_UNSUPPORTED;
+  if (a.d_h > 256 || a.d_vh > 256) return MHA_ERR_UNSUPPORTED;
   AttnParams P;
   P.Q = a.Q;
   P.K = a.K;
@@ -261,23 +277,18 @@ mha_status attention_simt(const AttnArgs& a, mha_dtype dt, cudaStream_t s) {
   P.pad_queries = a.pad_queries;
   for (int b = 0; b < MHA_MAX_PADDED_BATCH; ++b)
     P.valid_len[b] = (a.padding && b < a.B) ? a.valid_len_host[b] : a.n_k;
+  for (int i = 0; i < MHA_MAX_GATED_HEADS; ++i)
+    P.head_gate[i] = (a.head_gate_host && i < a.h) ? a.head_gate_host[i] : 1.f;
   const size_t smem =
       sizeof(float) * (AT_ROWS * a.d_h + AT_KEYS * (a.d_h + 1) + AT_KEYS * a.d_vh);
   const dim3 grid((a.n_q + AT_ROWS - 1) / AT_ROWS, a.h, a.B);
   if (grid.y > 65535u || grid.z > 65535u) return MHA_ERR_UNSUPPORTED;
-  cudaError_t e;
-  if (dt == MHA_DTYPE_F32) {
-    e = cudaFuncSetAttribute(attention_simt_kernel<float>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) attention_simt_kernel<float><<<grid, 256, smem, s>>>(P);
-  } else {
-    e = cudaFuncSetAttribute(attention_simt_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) attention_simt_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(P);
-  }
-  if (e != cudaSuccess) return MHA_ERR_CUDA;
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  const bool wide = a.d_vh > 128;
+  if (dt == MHA_DTYPE_F32)
+    return wide ? launch_attention_simt<float, 256>(P, grid, smem, s)
+                : launch_attention_simt<float, 128>(P, grid, smem, s);
+  return wide ? launch_attention_simt<__nv_bfloat16, 256>(P, grid, smem, s)
+              : launch_attention_simt<__nv_bfloat16, 128>(P, grid, smem, s);
 }
 
 }  // namespace mha

@@ -33,7 +33,7 @@ EXPORTS = (
     "mha_workspace_size", "mha_workspace_layout", "mha_forward", "mha_qkv_projection", "mha_attention",
     "mha_output_projection", "mha_get_device_error", "mha_status_string",
     "mha_selftest_wait_timeout", "mha_kernel_launch_count", "mha_version",
-    "mha_forward_no_alloc",
+    "mha_forward_no_alloc", "mha_forward_general",
 )
 
 _lib = None
@@ -61,6 +61,8 @@ def load(path=LIB_PATH):
     lib.mha_workspace_layout.argtypes = [I] * 6 + [I, ctypes.POINTER(S)]
     lib.mha_forward.restype = I
     lib.mha_forward.argtypes = [P] * 7 + [I] * 8 + [F, I, P, I, P, S, P]
+    lib.mha_forward_general.restype = I
+    lib.mha_forward_general.argtypes = [P] * 8 + [I] * 10 + [F, I, P, I, P, I, P, S, P]
     lib.mha_forward_no_alloc.restype = I
     lib.mha_forward_no_alloc.argtypes = [P] * 7 + [I] * 8 + [F, I, P, I, P]
     lib.mha_qkv_projection.restype = I
@@ -158,6 +160,43 @@ def forward(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, mask="none", valid_l
     _check(st, "mha_forward")
     if check:
         _check(lib.mha_get_device_error(_ptr(workspace), _stream(stream)), "mha_forward (device)")
+    return out
+
+
+def forward_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, mask="none",
+                    valid_len=None, self_attention=False, head_gate=None, out=None,
+                    workspace=None, stream=None, check=True):
+    """mha_forward_general: separate query, key and value inputs of their own
+    widths, X_q (B, n_q, d_q), X_k (B, n_k, d_k), X_v (B, n_k, d_v); head_gate
+    (h floats, or None) scales each head's output block before W_O (0 ablates
+    the head). Returns Y (B, n_q, d_o)."""
+    lib = load()
+    B, n_q, d_q = X_q.shape
+    n_k, d_k = X_k.shape[1], X_k.shape[2]
+    d_v = X_v.shape[2]
+    d_o = W_O.shape[1]
+    dt = TORCH_DTYPES[X_q.dtype]
+    if out is None:
+        out = torch.empty((B, n_q, d_o), dtype=X_q.dtype, device=X_q.device)
+    ws_bytes = workspace_size(B, n_q, n_k, d_q, h, d_h, d_vh, d_o, dt)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=X_q.device)
+    lens, keep = _lens(valid_len, B)
+    gate = None
+    if head_gate is not None:
+        gate = (ctypes.c_float * h)(*[float(x) for x in head_gate])
+    st = lib.mha_forward_general(_ptr(X_q), _ptr(X_k), _ptr(X_v), _ptr(W_Q), _ptr(W_K),
+                                 _ptr(W_V), _ptr(W_O), _ptr(out), B, n_q, n_k, d_q, d_k, d_v, h,
+                                 d_h, d_vh, d_o, float(c), MASKS[mask], lens,
+                                 int(bool(self_attention)),
+                                 None if gate is None else ctypes.cast(gate, ctypes.c_void_p),
+                                 DTYPES[dt], _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    del keep, gate
+    _check(st, "mha_forward_general")
+    if check:
+        _check(lib.mha_get_device_error(_ptr(workspace), _stream(stream)),
+               "mha_forward_general (device)")
     return out
 
 

@@ -96,6 +96,9 @@ typedef enum { MHA_DTYPE_F32 = 0, MHA_DTYPE_BF16 = 1 } mha_dtype;
  * travel to the kernels inside their launch parameters). */
 #define MHA_MAX_PADDED_BATCH 1024
 
+/* Most heads a head gate (mha_forward_general) may address. */
+#define MHA_MAX_GATED_HEADS 1024
+
 /*
  * Bytes of device workspace mha_forward needs for these sizes: the head-split
  * Q, K (B*h*n*d_h elements), V (B*h*n_k*d_vh), the concatenated Z
@@ -131,8 +134,9 @@ MHA_API mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h,
  *                                mha_workspace_size(...) bytes, 256-byte
  *                                aligned; its contents on entry do not matter
  *
- * bf16 limits (MHA_ERR_UNSUPPORTED otherwise): d_h and d_vh in {64, 128};
- * d_model and d_o multiples of 8. f32 limits: d_h, d_vh <= 128.
+ * Head sizes d_h, d_vh from 1 to 256 (MHA_ERR_UNSUPPORTED otherwise); bf16
+ * heads of 64 or 128 run on the tensor cores, other sizes on CUDA cores.
+ * bf16 also needs d_model, d_h, d_vh and d_o to be multiples of 8.
  * Enqueues a 4-byte memset of the error word and three kernels.
  */
 MHA_API mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q,
@@ -141,6 +145,50 @@ MHA_API mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_
                        int d_h, int d_vh, int d_o, float c, mha_mask_kind mask,
                        const int32_t* valid_len, mha_dtype dt, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/*
+ * The forward pass in the general form of "Multi-head attention and
+ * self-attention" (alphabetamath.cc, Definition): query, key and value
+ * inputs are three matrices of their own widths,
+ *   head i = Attn(X_q W_i^Q, X_k W_i^K, X_v W_i^V),  Y = Concat(heads) W^O.
+ *
+ *   X_q (B, n_q, d_q), X_k (B, n_k, d_k), X_v (B, n_k, d_v); X_k and X_v may
+ *                                be the same buffer, and so may X_q (self-
+ *                                attention passes X_q three times)
+ *   W_Q (d_q, h*d_h), W_K (d_k, h*d_h), W_V (d_v, h*d_vh), W_O (h*d_vh, d_o)
+ *   Y (B, n_q, d_o)
+ *   self_attention != 0          rows i >= valid_len[b] are padding queries
+ *                                (not computed, Y rows 0); needs n_q == n_k.
+ *                                0: a padding mask applies to keys only
+ *   head_gate                    HOST float[h] or NULL: head i's output block
+ *                                of the concatenation (columns [i*d_vh,
+ *                                (i+1)*d_vh) of Z, before W^O) is multiplied
+ *                                by head_gate[i]; 0 ablates the head, which
+ *                                equals zeroing row block i of W^O ("Head
+ *                                Identity and Ablation", Multi-Head Attention
+ *                                review). NULL: every gate is 1. With a gate,
+ *                                h <= MHA_MAX_GATED_HEADS (else
+ *                                MHA_ERR_UNSUPPORTED); gates must be finite
+ *                                (else MHA_ERR_INVALID_ARG)
+ *   workspace                    as for mha_forward (mha_workspace_size with
+ *                                any d_model: the intermediates do not depend
+ *                                on the input widths)
+ *
+ * Head sizes d_h, d_vh from 1 to 256; bf16 heads of 64 or 128 run on the
+ * tensor cores, other sizes on CUDA cores. bf16 also needs d_q, d_k, d_v,
+ * d_h, d_vh and d_o to be multiples of 8 and 16-byte aligned pointers
+ * (MHA_ERR_UNSUPPORTED otherwise). Other errors as for mha_forward.
+ * mha_forward is this call with X_k = X_v = X_kv (or X_q) and
+ * d_q = d_k = d_v = d_model.
+ */
+MHA_API mha_status mha_forward_general(const void* X_q, const void* X_k, const void* X_v,
+                                       const void* W_Q, const void* W_K, const void* W_V,
+                                       const void* W_O, void* Y, int B, int n_q, int n_k,
+                                       int d_q, int d_k, int d_v, int h, int d_h, int d_vh,
+                                       int d_o, float c, mha_mask_kind mask,
+                                       const int32_t* valid_len, int self_attention,
+                                       const float* head_gate, mha_dtype dt, void* workspace,
+                                       size_t workspace_bytes, void* stream);
 
 /*
  * Step 1: combined projections with the head split ("Separate and Combined

@@ -229,31 +229,41 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def mha_forward(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c,
-                mask=MASK_NONE, valid_len=None, return_intermediates=False):
-    """Y = Concat_i(softmax(c (X_q W_i^Q)(X_kv W_i^K)^T + M)(X_kv W_i^V)) W_O.
+def mha_forward_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c,
+                        mask=MASK_NONE, valid_len=None, self_attention=False,
+                        head_gate=None, return_intermediates=False):
+    """The general form of the 'Multi-head attention and self-attention'
+    Definition: query, key and value inputs are separate matrices, each with
+    its own width,
+        head i = Attn(X_q W_i^Q, X_k W_i^K, X_v W_i^V),
+        Y = Concat_feature(head_1 .. head_h) W^O.
 
     Batch-major arguments, all converted to float64:
-      X_q  (B, n_q, d_model); X_kv (B, n_k, d_model) or None for
-      self-attention (X_kv := X_q);
-      W_Q, W_K (d_model, h*d_h); W_V (d_model, h*d_vh): head i owns the
+      X_q (B, n_q, d_q); X_k (B, n_k, d_k); X_v (B, n_k, d_v);
+      W_Q (d_q, h*d_h), W_K (d_k, h*d_h), W_V (d_v, h*d_vh): head i owns the
       column block [i*d, (i+1)*d) (combined projections);
       W_O (h*d_vh, d_o): row block [i*d_vh, (i+1)*d_vh) belongs to head i;
-      valid_len: B integers for the padding masks, else None.
+      valid_len: B integers for the padding masks, else None;
+      self_attention: the query rows are positions of the same sequence, so
+      rows i >= valid_len are padding queries (their output rows are 0);
+      head_gate: h numbers or None. Head i's block of the concatenation is
+      multiplied by head_gate[i] before W_O: the head-zeroing location of the
+      'Multi-Head Attention review' ("Head Identity and Ablation", "Audit
+      Order": head zeroing at an explicitly named location).
 
     Returns Y (B, n_q, d_o) and, when asked, a dict with the head-split
     Q, K (B, h, n, d_h), V (B, h, n_k, d_vh) and the concatenated
-    Z (B, n_q, h*d_vh). Padded query rows (self-attention with padding) are 0.
+    Z (B, n_q, h*d_vh).
     """
-    self_attention = X_kv is None
-    X_q = _f64(X_q)
-    X_kv = X_q if self_attention else _f64(X_kv)
+    X_q, X_k, X_v = _f64(X_q), _f64(X_k), _f64(X_v)
     W_Q, W_K, W_V, W_O = _f64(W_Q), _f64(W_K), _f64(W_V), _f64(W_O)
-    B, n_q, d_model = X_q.shape
-    n_k = X_kv.shape[1]
+    B, n_q, d_q = X_q.shape
+    n_k, d_k = X_k.shape[1], X_k.shape[2]
+    d_v = X_v.shape[2]
     d_o = W_O.shape[1]
-    assert W_Q.shape == (d_model, h * d_h) and W_K.shape == (d_model, h * d_h)
-    assert W_V.shape == (d_model, h * d_vh) and W_O.shape == (h * d_vh, d_o)
+    assert X_k.shape[0] == B and X_v.shape[:2] == (B, n_k)
+    assert W_Q.shape == (d_q, h * d_h) and W_K.shape == (d_k, h * d_h)
+    assert W_V.shape == (d_v, h * d_vh) and W_O.shape == (h * d_vh, d_o)
     if _has_padding(mask):
         if valid_len is None or len(valid_len) != B:
             raise ValueError("a padding mask needs one valid length per batch item")
@@ -271,19 +281,32 @@ def mha_forward(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c,
         allowed = allowed_keys(mask, n_q, n_k, L)
         # combined projections, then the head split (B,T,h d)->(B,T,h,d)->(B,h,T,d)
         Qb = (X_q[b] @ W_Q).reshape(n_q, h, d_h).transpose(1, 0, 2)
-        Kb = (X_kv[b] @ W_K).reshape(n_k, h, d_h).transpose(1, 0, 2)
-        Vb = (X_kv[b] @ W_V).reshape(n_k, h, d_vh).transpose(1, 0, 2)
+        Kb = (X_k[b] @ W_K).reshape(n_k, h, d_h).transpose(1, 0, 2)
+        Vb = (X_v[b] @ W_V).reshape(n_k, h, d_vh).transpose(1, 0, 2)
         Qh[b], Kh[b], Vh[b] = Qb, Kb, Vb
         heads = []
         for i in range(h):
             H_i, _ = attention(Qb[i], Kb[i], Vb[i], c, allowed, rows)
             heads.append(H_i)
+        if head_gate is not None:
+            heads = [float(head_gate[i]) * heads[i] for i in range(h)]
         # concatenate along the feature axis in head order
         Z[b] = np.concatenate(heads, axis=1)
     Y = Z @ W_O
     if return_intermediates:
         return Y, {"Q": Qh, "K": Kh, "V": Vh, "Z": Z}
     return Y
+
+
+def mha_forward(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c,
+                mask=MASK_NONE, valid_len=None, return_intermediates=False):
+    """Y = Concat_i(softmax(c (X_q W_i^Q)(X_kv W_i^K)^T + M)(X_kv W_i^V)) W_O:
+    mha_forward_general with one key/value input X_kv (B, n_k, d_model), or
+    X_kv None for self-attention (X_kv := X_q, padded query rows are 0)."""
+    self_attention = X_kv is None
+    X_kv = X_q if self_attention else X_kv
+    return mha_forward_general(X_q, X_kv, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, mask,
+                               valid_len, self_attention, None, return_intermediates)
 
 
 def mha_forward_separate(X_q, X_kv, W_Q_list, W_K_list, W_V_list, W_O, c,

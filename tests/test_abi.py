@@ -88,8 +88,9 @@ def _lens(*v):
     (dict(n_k=65), 1),                       # self-attention needs n_k == n_q
     (dict(X_kv=28672, n_k=65, mask=1), 1),   # causal needs n_q == n_k
     (dict(mask=2), 1),                       # padding without valid lengths
-    (dict(d_h=96), 2), (dict(d_vh=32), 2), (dict(d_model=100), 2), (dict(d_o=12), 2),
-    (dict(d_h=192, dt=0), 2),
+    (dict(d_h=300), 2), (dict(d_vh=257), 2), (dict(d_model=100), 2), (dict(d_o=12), 2),
+    (dict(d_h=33), 2),                       # bf16: h*d_h must be a multiple of 8
+    (dict(d_h=300, dt=0), 2),
     (dict(X_q=4097), 2),                     # bf16 pointers must be 16-byte aligned
     (dict(ws=None), 4), (dict(ws=(1 << 20) + 16), 4), (dict(ws_bytes=1000), 4),
 ])
@@ -121,3 +122,41 @@ def test_steps_reject_bad_arguments_on_host(lib):
                                   9, 64, 1, 64, 64, 1, None, None) == 1
     assert lib.mha_get_device_error(None, None) == 1
     assert lib.mha_selftest_wait_timeout(None, 1000, None) == 1
+
+
+def _gen(lib, **kw):
+    """mha_forward_general with fake pointers; every call here must be rejected
+    by the host checks."""
+    a = dict(X_q=4096, X_k=28672, X_v=32768, W_Q=8192, W_K=12288, W_V=16384, W_O=20480,
+             Y=24576, B=2, n_q=64, n_k=80, d_q=128, d_k=96, d_v=40, h=2, d_h=64, d_vh=64,
+             d_o=128, c=0.125, mask=0, valid_len=None, self_attention=0, gate=None, dt=1,
+             ws=1 << 20, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.mha_forward_general(
+        P(a["X_q"]), P(a["X_k"]), P(a["X_v"]), P(a["W_Q"]), P(a["W_K"]), P(a["W_V"]),
+        P(a["W_O"]), P(a["Y"]), a["B"], a["n_q"], a["n_k"], a["d_q"], a["d_k"], a["d_v"], a["h"],
+        a["d_h"], a["d_vh"], a["d_o"], a["c"], a["mask"], a["valid_len"], a["self_attention"],
+        a["gate"], a["dt"], P(a["ws"]), a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(X_k=None), 1), (dict(X_v=None), 1), (dict(W_V=None), 1),
+    (dict(d_q=0), 1), (dict(d_k=-2), 1), (dict(d_v=0), 1),
+    (dict(self_attention=1), 1),             # self-attention needs n_q == n_k
+    (dict(mask=1), 1),                       # causal needs n_q == n_k
+    (dict(d_v=36), 2),                       # bf16 input widths: multiples of 8
+    (dict(d_k=100), 2),
+    (dict(d_h=260), 2),
+    (dict(X_v=32776), 2),                    # bf16 pointers must be 16-byte aligned
+    (dict(ws_bytes=10), 4),
+])
+def test_general_forward_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _gen(lib, **kw) == code
+
+
+def test_head_gates_must_be_finite_and_few_enough(lib):
+    bad = (ctypes.c_float * 2)(1.0, math.nan)
+    assert _gen(lib, gate=ctypes.cast(bad, ctypes.c_void_p)) == 1
+    many = (ctypes.c_float * 1025)(*([1.0] * 1025))
+    assert _gen(lib, gate=ctypes.cast(many, ctypes.c_void_p), h=1025, d_h=8, d_vh=8) == 2

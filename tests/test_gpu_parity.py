@@ -232,3 +232,86 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     w = workloads.WORKLOADS[1].with_(B=1, n_q=128, n_k=128)
     inp = workloads.make_inputs(w)
     check_full(w, inp, run(w, inp))
+
+
+# ---------------------------------------------------------------------------
+# The general form: separate key and value inputs of their own widths, and
+# head sizes beyond 64 / 128 ("Multi-head attention and self-attention",
+# Definition)
+# ---------------------------------------------------------------------------
+
+GENERAL = [
+    # B, n_q, n_k, d_q, d_k, d_v, h, d_h, d_vh, d_o, mask, self_attention, lens
+    (2, 130, 200, 64, 96, 40, 3, 64, 64, 72, "padding", False, [1, 200]),   # tensor cores
+    (2, 150, 150, 64, 64, 64, 2, 128, 64, 64, "causal", True, None),        # tensor cores
+    (2, 77, 140, 48, 32, 56, 3, 32, 48, 40, "none", False, None),          # CUDA cores
+    (1, 100, 100, 96, 96, 96, 2, 96, 96, 96, "causal_padding", True, [61]),
+    (1, 70, 90, 256, 128, 64, 2, 256, 256, 64, "padding", False, [45]),     # d = 256
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", GENERAL, ids=lambda s: "x".join(map(str, s[:10])) + "_" + s[10])
+def test_general_form(shape, dtype):
+    B, n_q, n_k, d_q, d_k, d_v, h, d_h, d_vh, d_o, mask, self_attn, lens = shape
+    g = torch.Generator().manual_seed(n_q * 7 + d_h)
+    tdt = workloads.torch_dtype(dtype)
+    rnd = lambda *s, scale=1.0: (torch.randn(s, generator=g) * scale).to(tdt)
+    X_q = rnd(B, n_q, d_q)
+    if self_attn:
+        X_k = X_v = X_q
+    else:
+        X_k, X_v = rnd(B, n_k, d_k), rnd(B, n_k, d_v)
+    W_Q = rnd(d_q, h * d_h, scale=d_q ** -0.5)
+    W_K = rnd(d_k, h * d_h, scale=d_k ** -0.5)
+    W_V = rnd(d_v, h * d_vh, scale=d_v ** -0.5)
+    W_O = rnd(h * d_vh, d_o, scale=(h * d_vh) ** -0.5)
+    c = 1 / math.sqrt(d_h)
+    dev = lambda t: t.cuda()
+    Y = mha.forward_general(dev(X_q), dev(X_k), dev(X_v), dev(W_Q), dev(W_K), dev(W_V),
+                            dev(W_O), h, d_h, d_vh, c, mask, lens, self_attention=self_attn)
+    torch.cuda.synchronize()
+    ref = oracle.mha_forward_general(f64(X_q), f64(X_k), f64(X_v), f64(W_Q), f64(W_K), f64(W_V),
+                                     f64(W_O), h, d_h, d_vh, c, oracle.MASK_NAMES[mask], lens,
+                                     self_attn)
+    got = f64(Y)
+    assert np.isfinite(got).all()
+    rows = np.ones((B, n_q), dtype=bool)
+    if self_attn and lens is not None:
+        for b in range(B):
+            rows[b, lens[b]:] = False
+        assert np.all(got[~rows] == 0.0)
+    assert rel_err(got[rows], ref[rows]) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 96), ("f32", 64)])
+def test_head_gate_zeroes_a_head_like_its_w_o_block(dtype, d):
+    """Head zeroing at the named location (the head's block of the
+    concatenation, before W_O) equals zeroing that head's rows of W_O, and the
+    gates match the oracle's."""
+    B, n, d_model, h = 2, 140, 128, 4
+    g = torch.Generator().manual_seed(300 + d)
+    tdt = workloads.torch_dtype(dtype)
+    rnd = lambda *s, scale=1.0: (torch.randn(s, generator=g) * scale).to(tdt)
+    X = rnd(B, n, d_model)
+    W_Q, W_K = rnd(d_model, h * d, scale=d_model ** -0.5), rnd(d_model, h * d, scale=d_model ** -0.5)
+    W_V = rnd(d_model, h * d, scale=d_model ** -0.5)
+    W_O = rnd(h * d, d_model, scale=(h * d) ** -0.5)
+    gate = [1.0, 0.0, 0.5, 1.0]
+    c = 1 / math.sqrt(d)
+    dev = lambda t: t.cuda()
+    Yg = mha.forward_general(dev(X), dev(X), dev(X), dev(W_Q), dev(W_K), dev(W_V), dev(W_O), h, d,
+                             d, c, "causal", None, self_attention=True, head_gate=gate)
+    W_O0 = W_O.clone()
+    W_O0[d:2 * d] = 0
+    Yw = mha.forward_general(dev(X), dev(X), dev(X), dev(W_Q), dev(W_K), dev(W_V), dev(W_O0),
+                             h, d, d, c, "causal", None, self_attention=True,
+                             head_gate=[1.0, 1.0, 0.5, 1.0])
+    torch.cuda.synchronize()
+    ref = oracle.mha_forward_general(f64(X), f64(X), f64(X), f64(W_Q), f64(W_K), f64(W_V),
+                                     f64(W_O), h, d, d, c, oracle.MASK_CAUSAL, None, True,
+                                     head_gate=gate)
+    assert rel_err(f64(Yg), ref) <= TOL[dtype]
+    # zeroing by gate or by W_O rows: the Z blocks that reach W_O differ only
+    # in head 1, whose W_O rows are zero in the second call
+    assert rel_err(f64(Yg), f64(Yw)) <= TOL[dtype]

@@ -377,3 +377,156 @@ def test_brute_force_tiny(case):
     ref = _brute(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, 0.75,
                  (lambda b, i, j: j <= i) if kind == "causal" else (lambda b, i, j: True))
     np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# The general form: separate query, key and value inputs of their own widths
+# ("Multi-head attention and self-attention", Definition: Q in R^{n_q x d_q},
+# K in R^{n_k x d_k}, V in R^{n_k x d_v})
+# ---------------------------------------------------------------------------
+
+def rand_general(seed, B, n_q, n_k, d_q, d_k, d_v, h, d_h, d_vh, d_o):
+    r = rng(seed)
+    X_q = r.standard_normal((B, n_q, d_q))
+    X_k = r.standard_normal((B, n_k, d_k))
+    X_v = r.standard_normal((B, n_k, d_v))
+    W_Q = r.standard_normal((d_q, h * d_h)) / math.sqrt(d_q)
+    W_K = r.standard_normal((d_k, h * d_h)) / math.sqrt(d_k)
+    W_V = r.standard_normal((d_v, h * d_vh)) / math.sqrt(d_v)
+    W_O = r.standard_normal((h * d_vh, d_o)) / math.sqrt(h * d_vh)
+    return X_q, X_k, X_v, W_Q, W_K, W_V, W_O
+
+
+def _brute_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, allowed_fn):
+    B, n_q, d_q = X_q.shape
+    n_k, d_k, d_v = X_k.shape[1], X_k.shape[2], X_v.shape[2]
+    d_o = W_O.shape[1]
+    Y = np.zeros((B, n_q, d_o))
+    for b in range(B):
+        for i in range(n_q):
+            z = []
+            for hd in range(h):
+                q = [math.fsum(X_q[b, i, t] * W_Q[t, hd * d_h + r] for t in range(d_q))
+                     for r in range(d_h)]
+                keys = [j for j in range(n_k) if allowed_fn(b, i, j)]
+                s = {}
+                for j in keys:
+                    k = [math.fsum(X_k[b, j, t] * W_K[t, hd * d_h + r] for t in range(d_k))
+                         for r in range(d_h)]
+                    s[j] = c * math.fsum(q[r] * k[r] for r in range(d_h))
+                m = max(s.values())
+                e = {j: math.exp(s[j] - m) for j in keys}
+                tot = math.fsum(e.values())
+                for r in range(d_vh):
+                    vr = {j: math.fsum(X_v[b, j, t] * W_V[t, hd * d_vh + r] for t in range(d_v))
+                          for j in keys}
+                    z.append(math.fsum(e[j] * vr[j] for j in keys) / tot)
+            for o in range(d_o):
+                Y[b, i, o] = math.fsum(z[f] * W_O[f, o] for f in range(len(z)))
+    return Y
+
+
+@pytest.mark.parametrize("kind", ["none", "causal", "padding"])
+def test_general_form_brute_force_tiny(kind):
+    h, d_h, d_vh = 2, 3, 2
+    n_q, n_k = (3, 3) if kind == "causal" else (3, 4)
+    X_q, X_k, X_v, W_Q, W_K, W_V, W_O = rand_general(
+        140 + len(kind), B=2, n_q=n_q, n_k=n_k, d_q=3, d_k=4, d_v=2, h=h, d_h=d_h, d_vh=d_vh,
+        d_o=3)
+    mask = {"none": O.MASK_NONE, "causal": O.MASK_CAUSAL, "padding": O.MASK_PADDING}[kind]
+    valid_len = [2, 4] if kind == "padding" else None
+    Y = O.mha_forward_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, h, d_h, d_vh, 0.8, mask,
+                              valid_len)
+    if kind == "causal":
+        fn = lambda b, i, j: j <= i
+    elif kind == "padding":
+        fn = lambda b, i, j: j < valid_len[b]
+    else:
+        fn = lambda b, i, j: True
+    ref = _brute_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, h, d_h, d_vh, 0.8, fn)
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("mask", [O.MASK_NONE, O.MASK_CAUSAL, O.MASK_PADDING])
+def test_general_form_matches_torch_with_separate_key_and_value_inputs(mask):
+    """torch's multi-head attention takes key and value tensors of their own
+    widths (kdim, vdim); its query width, head sizes and output width are tied
+    to embed_dim = h d_h, so those are chosen that way here."""
+    h, d_h = 3, 4
+    E = h * d_h
+    B, n = 2, 6
+    d_k, d_v = 7, 5
+    X_q, X_k, X_v, W_Q, W_K, W_V, W_O = rand_general(
+        150 + mask, B=B, n_q=n, n_k=n, d_q=E, d_k=d_k, d_v=d_v, h=h, d_h=d_h, d_vh=d_h, d_o=E)
+    c = 0.47
+    valid_len = [6, 2] if mask == O.MASK_PADDING else None
+    Y = O.mha_forward_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, h, d_h, d_h, c, mask,
+                              valid_len)
+    Xq = torch.from_numpy(X_q).transpose(0, 1)
+    Xk = torch.from_numpy(X_k).transpose(0, 1)
+    Xv = torch.from_numpy(X_v).transpose(0, 1)
+    attn_mask = torch.ones(n, n, dtype=torch.bool).triu(1) if mask == O.MASK_CAUSAL else None
+    kpm = None
+    if mask == O.MASK_PADDING:
+        kpm = torch.arange(n)[None, :] >= torch.as_tensor(valid_len)[:, None]
+    out, _ = torch.nn.functional.multi_head_attention_forward(
+        Xq, Xk, Xv, E, h, None, None, None, None, False, 0.0,
+        torch.from_numpy(W_O).T.contiguous(), None, training=False, key_padding_mask=kpm,
+        need_weights=False, attn_mask=attn_mask, use_separate_proj_weight=True,
+        q_proj_weight=torch.from_numpy(W_Q * (c * math.sqrt(d_h))).T.contiguous(),
+        k_proj_weight=torch.from_numpy(W_K).T.contiguous(),
+        v_proj_weight=torch.from_numpy(W_V).T.contiguous())
+    np.testing.assert_allclose(Y, out.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_general_form_key_and_value_inputs_are_not_interchangeable():
+    """With d_k == d_v, swapping the key and value inputs must change the output
+    (the keys decide the weights, the values what is averaged)."""
+    X_q, X_k, X_v, W_Q, W_K, W_V, W_O = rand_general(
+        160, B=1, n_q=4, n_k=5, d_q=6, d_k=6, d_v=6, h=2, d_h=3, d_vh=3, d_o=4)
+    Y1 = O.mha_forward_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, 2, 3, 3, 0.9)
+    Y2 = O.mha_forward_general(X_q, X_v, X_k, W_Q, W_K, W_V, W_O, 2, 3, 3, 0.9)
+    assert np.abs(Y1 - Y2).max() > 1e-3
+
+
+def test_one_key_value_input_is_the_shared_case():
+    """mha_forward with X_kv equals the general form with X_k = X_v = X_kv."""
+    X_q, X_kv, W_Q, W_K, W_V, W_O = rand_layer(170, cross=True, n_k=9)
+    Y = O.mha_forward(X_q, X_kv, W_Q, W_K, W_V, W_O, 3, 4, 4, 0.5)
+    G = O.mha_forward_general(X_q, X_kv, X_kv, W_Q, W_K, W_V, W_O, 3, 4, 4, 0.5)
+    np.testing.assert_array_equal(Y, G)
+
+
+# ---------------------------------------------------------------------------
+# Head zeroing at a named location ("Multi-Head Attention review", "Head
+# Identity and Ablation" and "Audit Order"): the gate scales head i's block of
+# the concatenation, before W_O
+# ---------------------------------------------------------------------------
+
+def test_zeroing_a_head_gate_equals_zeroing_its_w_o_row_block():
+    h, d_h, d_vh = 3, 4, 5
+    X_q, X_k, X_v, W_Q, W_K, W_V, W_O = rand_general(
+        180, B=2, n_q=6, n_k=7, d_q=5, d_k=6, d_v=4, h=h, d_h=d_h, d_vh=d_vh, d_o=8)
+    for i in range(h):
+        gate = [1.0] * h
+        gate[i] = 0.0
+        Yg = O.mha_forward_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, h, d_h, d_vh, 0.7,
+                                   head_gate=gate)
+        W_O0 = W_O.copy()
+        W_O0[i * d_vh:(i + 1) * d_vh] = 0.0
+        Yw = O.mha_forward_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O0, h, d_h, d_vh, 0.7)
+        np.testing.assert_allclose(Yg, Yw, rtol=1e-13, atol=1e-15)
+
+
+def test_head_gates_scale_each_heads_contribution_linearly():
+    h, d_h, d_vh = 2, 3, 3
+    X_q, X_k, X_v, W_Q, W_K, W_V, W_O = rand_general(
+        181, B=1, n_q=5, n_k=5, d_q=4, d_k=4, d_v=4, h=h, d_h=d_h, d_vh=d_vh, d_o=4)
+    f = lambda g: O.mha_forward_general(X_q, X_k, X_v, W_Q, W_K, W_V, W_O, h, d_h, d_vh, 0.5,
+                                        O.MASK_CAUSAL, head_gate=g)
+    np.testing.assert_allclose(f([1.0, 1.0]), f(None), rtol=0, atol=0)
+    np.testing.assert_allclose(f([1.0, 1.0]), f([1.0, 0.0]) + f([0.0, 1.0]), rtol=1e-13,
+                               atol=1e-15)
+    np.testing.assert_allclose(f([2.5, -1.0]), 2.5 * f([1.0, 0.0]) - f([0.0, 1.0]),
+                               rtol=1e-12, atol=1e-14)
+    assert np.all(f([0.0, 0.0]) == 0.0)
