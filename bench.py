@@ -300,6 +300,57 @@ def measure_e2e(w, inp, t, steps, warmup, dev, world, ws, flush):
     return {"ms": tot, "h2d": h2d, "d2h": d2h}
 
 
+def decode_bytes(w, lens):
+    """Algorithmic bytes of one decode launch: the valid part of K and V read
+    once, Q read, Z written (the partial summaries are not counted)."""
+    es = 2 if w.dtype == "bf16" else 4
+    kv = sum(lens) * w.h * (w.d_h + w.d_vh) * es
+    return kv + w.B * w.h * w.n_q * (w.d_h + w.d_vh) * es
+
+
+def measure_decode(w, steps, warmup, dev, pk):
+    """Times mha_attention_decode on the decode workload: inputs resident in
+    HBM, L2 flushed between timed launches (outside the events)."""
+    import torch
+
+    from head_scaled_dot_gb300 import mha, workloads
+    inp = workloads.make_decode_inputs(w)
+    Q, K, V = (inp[k].to(dev) for k in ("Q", "K", "V"))
+    lens = inp["cache_len"]
+    Z = torch.empty((w.B, w.n_q, w.h * w.d_vh), dtype=Q.dtype, device=dev)
+    ws = torch.empty(mha.decode_workspace_size(w.B, w.n_q, w.n_k, w.h, w.d_vh),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        mha.attention_decode(Q, K, V, w.c, lens, w.causal_tail, out=Z, workspace=ws,
+                             stream=stream)
+
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        one()
+    torch.cuda.synchronize(dev)
+    tot = 0.0
+    for _ in range(steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        tot += e0.elapsed_time(e1)
+    ms = tot / steps
+    nbytes = decode_bytes(w, lens)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms_per_launch": ms, "bytes_per_launch": nbytes,
+            "roofline": {"kernel": "decode (split summaries + merge)", "bound": "hbm",
+                         "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"]},
+            "config": {"B": w.B, "h": w.h, "n_q": w.n_q, "n_k": w.n_k, "d_h": w.d_h,
+                       "d_vh": w.d_vh, "cache_len": lens, "causal_tail": w.causal_tail}}
+
+
 def oracle_sample(w, inp, lens, unit):
     """Runs the oracle as it stands on one (batch item, head) unit of the
     workload: the head's projections, its dense attention and its share of
@@ -434,6 +485,8 @@ def run_ours(args):
                                "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
                                "kernels": kr}
             del r
+        dw = workloads.DECODE
+        others[dw.name] = measure_decode(dw, max(3, args.steps), 3, dev, pk)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, res["inputs"], res["lens"])

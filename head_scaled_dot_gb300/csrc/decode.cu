@@ -1,0 +1,527 @@
+// decode.cu - attention of a few query rows over a long key/value cache,
+// split over the keys and merged with the summary merge.
+//
+// "Stable summary of an attention key block" (alphabetamath.cc, Definition):
+// the summary (m, l, z) of a key set, and the merge of the summaries of two
+// disjoint sets, m' = max(m_S, m_T), l' = e^{m_S - m'} l_S + e^{m_T - m'} l_T,
+// z' likewise; z / l of the merged summary is the attention output over the
+// union. Here the keys of one (batch item, head) are cut into chunks of
+// DEC_CHUNK keys and each warp of a chunk's CTA folds a share of them, 32 at a
+// time, into its own summary (pass 1); pass 2 merges every partial summary of
+// a query row and writes z / l. Summaries are kept in base 2: scores are
+// pre-multiplied by c log2(e), which leaves z / l unchanged.
+//
+// The work is bound by reading K and V once (a handful of query rows), so it
+// runs on CUDA cores: lane j of a warp scores key j of a 32-key group against
+// every query row, the group's weights are shuffled across the lanes, and
+// each lane accumulates its own columns of z.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace mha {
+namespace {
+
+constexpr int DEC_THREADS = 256;
+constexpr int DEC_WARPS = DEC_THREADS / 32;
+#ifndef MHA_DECODE_CHUNK
+#define MHA_DECODE_CHUNK 1024
+#endif
+constexpr int DEC_CHUNK = MHA_DECODE_CHUNK;  // keys per CTA
+constexpr int DEC_NQ = 8;       // query rows per pass over the chunk
+#ifndef MHA_DECODE_VUNROLL
+#define MHA_DECODE_VUNROLL 4
+#endif
+constexpr int DEC_VUNROLL = MHA_DECODE_VUNROLL;  // value rows in flight per lane
+
+struct DecodeParams {
+  const void* Q;   // (B, h, n_q, d_h)
+  const void* K;   // (B, h, n_k, d_h)
+  const void* V;   // (B, h, n_k, d_vh)
+  void* Z;         // (B, n_q, h * d_vh)
+  float* part;     // [B][h][n_q][nsplit][2 + d_vh]: m, l, z of each warp's keys
+  int B, n_q, n_k, h, d_h, d_vh, nsplit;
+  float cl2;       // c * log2(e)
+  int causal_tail; // row i sees keys j <= L - n_q + i
+  int valid_len[MHA_MAX_PADDED_BATCH];
+};
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p);
+template <>
+__device__ __forceinline__ float ldf<float>(const float* p) {
+  return __ldg(p);
+}
+template <>
+__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+// Eight consecutive elements starting at a 16-byte aligned address.
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ float dwarp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float dwarp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Pass 1. grid (chunks, h, B). Warp w of chunk ch folds the keys
+// k0 + 32 (w + DEC_WARPS it) + lane, it = 0, 1, ... (below the chunk end and
+// the valid length) into one summary per query row, and writes it as split
+// ch * DEC_WARPS + w. VW: z columns per lane (d_vh <= 32 VW). VEC: d_h is a
+// multiple of 8 and K rows are 16-byte aligned (vector loads).
+template <typename T, int VW, bool VEC>
+__global__ void __launch_bounds__(DEC_THREADS) decode_partial_kernel(
+    const __grid_constant__ DecodeParams P) {
+  __shared__ __align__(16) float qs[DEC_NQ][256];
+  const int chunk = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int L = P.valid_len[b];
+  const int k0 = chunk * DEC_CHUNK;
+  if (k0 >= L) return;  // the merge reads only the splits below L
+  const int k1 = min(L, k0 + DEC_CHUNK);
+  const int dq = P.d_h, dv = P.d_vh;
+  const long long bh = (long long)b * P.h + head;
+  const T* Qg = static_cast<const T*>(P.Q) + bh * P.n_q * dq;
+  const T* Kg = static_cast<const T*>(P.K) + bh * P.n_k * dq;
+  const T* Vg = static_cast<const T*>(P.V) + bh * P.n_k * dv;
+  const int split = chunk * DEC_WARPS + warp;
+
+  for (int r0 = 0; r0 < P.n_q; r0 += DEC_NQ) {
+    const int nr = min(DEC_NQ, P.n_q - r0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < nr * dq; e += DEC_THREADS) {
+      const int r = e / dq, k = e % dq;
+      qs[r][k] = ldf(Qg + (long long)(r0 + r) * dq + k) * P.cl2;
+    }
+    __syncthreads();
+    float m_run[DEC_NQ], l_run[DEC_NQ], z_run[DEC_NQ][VW];
+#pragma unroll
+    for (int r = 0; r < DEC_NQ; ++r) {
+      m_run[r] = -INFINITY;
+      l_run[r] = 0.f;
+#pragma unroll
+      for (int t = 0; t < VW; ++t) z_run[r][t] = 0.f;
+    }
+    for (int g0 = k0 + 32 * warp; g0 < k1; g0 += 32 * DEC_WARPS) {
+      const int key = g0 + lane;
+      const bool in = key < k1;
+      // scores of this lane's key against every query row (already in log2 units)
+      float s[DEC_NQ];
+#pragma unroll
+      for (int r = 0; r < DEC_NQ; ++r) s[r] = 0.f;
+      if (in) {
+        const T* krow = Kg + (long long)key * dq;
+        if (VEC) {
+          // 8 elements per 16-byte load (two for fp32); rows are 16-byte aligned
+          for (int k = 0; k < dq; k += 8) {
+            float kv[8];
+            load8(krow + k, kv);
+#pragma unroll
+            for (int r = 0; r < DEC_NQ; ++r) {
+              const float4 q0 = *reinterpret_cast<const float4*>(&qs[r][k]);
+              const float4 q1 = *reinterpret_cast<const float4*>(&qs[r][k + 4]);
+              float acc = s[r];
+              acc = fmaf(q0.x, kv[0], acc);
+              acc = fmaf(q0.y, kv[1], acc);
+              acc = fmaf(q0.z, kv[2], acc);
+              acc = fmaf(q0.w, kv[3], acc);
+              acc = fmaf(q1.x, kv[4], acc);
+              acc = fmaf(q1.y, kv[5], acc);
+              acc = fmaf(q1.z, kv[6], acc);
+              acc = fmaf(q1.w, kv[7], acc);
+              s[r] = acc;
+            }
+          }
+        } else {
+          for (int k = 0; k < dq; ++k) {
+            const float kv = ldf(krow + k);
+#pragma unroll
+            for (int r = 0; r < DEC_NQ; ++r) s[r] = fmaf(qs[r][k], kv, s[r]);
+          }
+        }
+      }
+      float p[DEC_NQ];
+#pragma unroll
+      for (int r = 0; r < DEC_NQ; ++r) {
+        p[r] = 0.f;
+        if (r >= nr) continue;  // uniform
+        bool allowed = in;
+        if (P.causal_tail) allowed = allowed && key <= L - P.n_q + r0 + r;
+        const float sv = allowed ? s[r] : -INFINITY;
+        const float m_blk = dwarp_max(sv);
+        if (m_blk == -INFINITY) continue;  // no allowed key in this group: the empty summary
+        // merge the group's summary into the running one (base 2)
+        const float m_new = fmaxf(m_run[r], m_blk);
+        const float a = exp2f(m_run[r] - m_new);
+        p[r] = allowed ? exp2f(sv - m_new) : 0.f;
+        l_run[r] = l_run[r] * a + dwarp_sum(p[r]);
+#pragma unroll
+        for (int t = 0; t < VW; ++t) z_run[r][t] *= a;
+        m_run[r] = m_new;
+      }
+      // z += sum over the group's keys of p_j v_j; lane owns columns lane + 32 t
+      const int ng = min(32, k1 - g0);
+      for (int j = 0; j < ng; ++j) {
+        const T* vrow = Vg + (long long)(g0 + j) * dv;
+        float vv[VW];
+#pragma unroll
+        for (int t = 0; t < VW; ++t) {
+          const int col = lane + 32 * t;
+          vv[t] = col < dv ? ldf(vrow + col) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < DEC_NQ; ++r) {
+          const float pj = __shfl_sync(0xffffffffu, p[r], j);
+#pragma unroll
+          for (int t = 0; t < VW; ++t) z_run[r][t] = fmaf(pj, vv[t], z_run[r][t]);
+        }
+      }
+    }
+    // this warp's summaries of the group of rows
+#pragma unroll
+    for (int r = 0; r < DEC_NQ; ++r) {
+      if (r >= nr) continue;
+      float* dst = P.part + ((bh * P.n_q + r0 + r) * P.nsplit + split) * (long long)(2 + dv);
+      if (lane == 0) {
+        dst[0] = m_run[r];
+        dst[1] = l_run[r];
+      }
+#pragma unroll
+      for (int t = 0; t < VW; ++t) {
+        const int col = lane + 32 * t;
+        if (col < dv) dst[2 + col] = z_run[r][t];
+      }
+    }
+  }
+}
+
+// Raw words of a 16-byte chunk and their values: 8 bf16 or 4 fp32.
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void unpack(const uint4& u, float* v) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ static void unpack(const uint4& u, float* v) {
+    v[0] = __uint_as_float(u.x);
+    v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z);
+    v[3] = __uint_as_float(u.w);
+  }
+};
+
+// DV / 32 consecutive values of a row, as a lane's share of a warp-wide load.
+template <typename T, int CPL>
+__device__ __forceinline__ void load_cols(const T* p, float (&v)[CPL]) {
+  if constexpr (sizeof(T) == 2) {
+    static_assert(CPL == 2 || CPL == 4 || CPL == 8, "columns per lane");
+    if constexpr (CPL == 2) {
+      const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(p));
+      v[0] = __uint_as_float(u << 16);
+      v[1] = __uint_as_float(u & 0xffff0000u);
+    } else if constexpr (CPL == 4) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+      v[0] = __uint_as_float(u.x << 16);
+      v[1] = __uint_as_float(u.x & 0xffff0000u);
+      v[2] = __uint_as_float(u.y << 16);
+      v[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+      Vec16<__nv_bfloat16>::unpack(u, v);
+    }
+  } else {
+    static_assert(CPL == 2 || CPL == 4, "columns per lane");
+    if constexpr (CPL == 2) {
+      const float2 u = __ldg(reinterpret_cast<const float2*>(p));
+      v[0] = u.x;
+      v[1] = u.y;
+    } else {
+      const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+      v[0] = u.x;
+      v[1] = u.y;
+      v[2] = u.z;
+      v[3] = u.w;
+    }
+  }
+}
+
+// Pass 1 for head sizes known at compile time (d_h = DQK, d_vh = DV, both
+// multiples of 32 and of 8 elements per 16 bytes), NQ query rows per pass.
+// A lane issues every load of its key row before using any of them, and the
+// value rows are read as warp-wide vectors (lane owns columns
+// [lane*DV/32, (lane+1)*DV/32)), so many bytes are in flight per warp.
+template <typename T, int NQ, int DQK, int DV>
+__global__ void __launch_bounds__(DEC_THREADS) decode_partial_fast_kernel(
+    const __grid_constant__ DecodeParams P) {
+  constexpr int CPL = DV / 32;           // z columns per lane
+  constexpr int KV16 = DQK / Vec16<T>::N; // 16-byte chunks per key row
+  __shared__ __align__(16) float qs[NQ][DQK];
+  const int chunk = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int L = P.valid_len[b];
+  const int k0 = chunk * DEC_CHUNK;
+  if (k0 >= L) return;
+  const int k1 = min(L, k0 + DEC_CHUNK);
+  const long long bh = (long long)b * P.h + head;
+  const T* Qg = static_cast<const T*>(P.Q) + bh * P.n_q * DQK;
+  const T* Kg = static_cast<const T*>(P.K) + bh * P.n_k * DQK;
+  const T* Vg = static_cast<const T*>(P.V) + bh * P.n_k * DV;
+  const int split = chunk * DEC_WARPS + warp;
+
+  for (int r0 = 0; r0 < P.n_q; r0 += NQ) {
+    const int nr = min(NQ, P.n_q - r0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < NQ * DQK; e += DEC_THREADS) {
+      const int r = e / DQK, k = e % DQK;
+      qs[r][k] = r < nr ? ldf(Qg + (long long)(r0 + r) * DQK + k) * P.cl2 : 0.f;
+    }
+    __syncthreads();
+    float m_run[NQ], l_run[NQ], z_run[NQ][CPL];
+#pragma unroll
+    for (int r = 0; r < NQ; ++r) {
+      m_run[r] = -INFINITY;
+      l_run[r] = 0.f;
+#pragma unroll
+      for (int t = 0; t < CPL; ++t) z_run[r][t] = 0.f;
+    }
+    for (int g0 = k0 + 32 * warp; g0 < k1; g0 += 32 * DEC_WARPS) {
+      const int key = g0 + lane;
+      const bool in = key < k1;
+      float s[NQ];
+#pragma unroll
+      for (int r = 0; r < NQ; ++r) s[r] = 0.f;
+      if (in) {
+        const uint4* krow = reinterpret_cast<const uint4*>(Kg + (long long)key * DQK);
+        uint4 raw[KV16];
+#pragma unroll
+        for (int i = 0; i < KV16; ++i) raw[i] = __ldg(krow + i);
+#pragma unroll
+        for (int i = 0; i < KV16; ++i) {
+          float kv[Vec16<T>::N];
+          Vec16<T>::unpack(raw[i], kv);
+#pragma unroll
+          for (int r = 0; r < NQ; ++r) {
+#pragma unroll
+            for (int e = 0; e < Vec16<T>::N; ++e)
+              s[r] = fmaf(qs[r][i * Vec16<T>::N + e], kv[e], s[r]);
+          }
+        }
+      }
+      float p[NQ];
+#pragma unroll
+      for (int r = 0; r < NQ; ++r) {
+        p[r] = 0.f;
+        if (r >= nr) continue;  // uniform
+        bool allowed = in;
+        if (P.causal_tail) allowed = allowed && key <= L - P.n_q + r0 + r;
+        const float sv = allowed ? s[r] : -INFINITY;
+        const float m_blk = dwarp_max(sv);
+        if (m_blk == -INFINITY) continue;  // the empty summary
+        const float m_new = fmaxf(m_run[r], m_blk);
+        const float a = exp2f(m_run[r] - m_new);
+        p[r] = allowed ? exp2f(sv - m_new) : 0.f;
+        l_run[r] = l_run[r] * a + dwarp_sum(p[r]);
+#pragma unroll
+        for (int t = 0; t < CPL; ++t) z_run[r][t] *= a;
+        m_run[r] = m_new;
+      }
+      const int ng = min(32, k1 - g0);
+      const T* vbase = Vg + (long long)g0 * DV + lane * CPL;
+#pragma unroll DEC_VUNROLL
+      for (int j = 0; j < ng; ++j) {
+        float vv[CPL];
+        load_cols<T, CPL>(vbase + (long long)j * DV, vv);
+#pragma unroll
+        for (int r = 0; r < NQ; ++r) {
+          const float pj = __shfl_sync(0xffffffffu, p[r], j);
+#pragma unroll
+          for (int t = 0; t < CPL; ++t) z_run[r][t] = fmaf(pj, vv[t], z_run[r][t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < NQ; ++r) {
+      if (r >= nr) continue;
+      float* dst = P.part + ((bh * P.n_q + r0 + r) * P.nsplit + split) * (long long)(2 + DV);
+      if (lane == 0) {
+        dst[0] = m_run[r];
+        dst[1] = l_run[r];
+      }
+#pragma unroll
+      for (int t = 0; t < CPL; ++t) dst[2 + lane * CPL + t] = z_run[r][t];
+    }
+  }
+}
+
+// Pass 2. grid (n_q, h, B), 256 threads: merges the splits of one query row
+// (those below the valid length) and writes z / l.
+template <typename T>
+__global__ void __launch_bounds__(DEC_THREADS) decode_merge_kernel(
+    const __grid_constant__ DecodeParams P) {
+  __shared__ float w[1024];
+  __shared__ float red[DEC_WARPS];
+  __shared__ float bcast;
+  const int row = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
+  const int L = P.valid_len[b];
+  const int nsp = ((L + DEC_CHUNK - 1) / DEC_CHUNK) * DEC_WARPS;
+  const int dv = P.d_vh;
+  const long long bh = (long long)b * P.h + head;
+  const float* src = P.part + (bh * P.n_q + row) * P.nsplit * (long long)(2 + dv);
+  // M = max of the splits' m (empty splits have m = -inf)
+  float mx = -INFINITY;
+  for (int s = threadIdx.x; s < nsp; s += DEC_THREADS) mx = fmaxf(mx, src[(long long)s * (2 + dv)]);
+  mx = dwarp_max(mx);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = red[0];
+    for (int i = 1; i < DEC_WARPS; ++i) v = fmaxf(v, red[i]);
+    bcast = v;
+  }
+  __syncthreads();
+  const float M = bcast;
+  // weights e^{m_s - M} (base 2) and l = sum_s l_s e^{m_s - M}
+  float lsum = 0.f;
+  for (int s = threadIdx.x; s < nsp; s += DEC_THREADS) {
+    const float m = src[(long long)s * (2 + dv)];
+    const float ws = (m == -INFINITY) ? 0.f : exp2f(m - M);
+    w[s] = ws;
+    lsum += ws * src[(long long)s * (2 + dv) + 1];
+  }
+  lsum = dwarp_sum(lsum);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = lsum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = 0.f;
+    for (int i = 0; i < DEC_WARPS; ++i) v += red[i];
+    bcast = v;
+  }
+  __syncthreads();
+  const float inv = 1.f / bcast;
+  T* zrow = static_cast<T*>(P.Z) + ((long long)b * P.n_q + row) * (long long)P.h * dv +
+            (long long)head * dv;
+  for (int col = threadIdx.x; col < dv; col += DEC_THREADS) {
+    float za[4] = {0.f, 0.f, 0.f, 0.f};
+    int s = 0;
+    for (; s + 4 <= nsp; s += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        za[u] = fmaf(w[s + u], src[(long long)(s + u) * (2 + dv) + 2 + col], za[u]);
+    }
+    for (; s < nsp; ++s) za[0] = fmaf(w[s], src[(long long)s * (2 + dv) + 2 + col], za[0]);
+    const float z = (za[0] + za[1]) + (za[2] + za[3]);
+    if (sizeof(T) == 4)
+      reinterpret_cast<float*>(zrow)[col] = z * inv;
+    else
+      reinterpret_cast<__nv_bfloat16*>(zrow)[col] = __float2bfloat16_rn(z * inv);
+  }
+}
+
+template <typename T, int DQK, int DV>
+bool launch_fast(const DecodeParams& P, const dim3& g1, cudaStream_t s) {
+  if (P.d_h != DQK || P.d_vh != DV) return false;
+  if (P.n_q == 1)
+    decode_partial_fast_kernel<T, 1, DQK, DV><<<g1, DEC_THREADS, 0, s>>>(P);
+  else if (P.n_q == 2)
+    decode_partial_fast_kernel<T, 2, DQK, DV><<<g1, DEC_THREADS, 0, s>>>(P);
+  else if (P.n_q <= 4)
+    decode_partial_fast_kernel<T, 4, DQK, DV><<<g1, DEC_THREADS, 0, s>>>(P);
+  else
+    decode_partial_fast_kernel<T, 8, DQK, DV><<<g1, DEC_THREADS, 0, s>>>(P);
+  return true;
+}
+
+template <typename T>
+mha_status launch_decode(const DecodeParams& P, int nchunk, cudaStream_t s) {
+  const dim3 g1(nchunk, P.h, P.B), g2(P.n_q, P.h, P.B);
+  if (launch_fast<T, 64, 64>(P, g1, s) || launch_fast<T, 128, 128>(P, g1, s)) {
+    decode_merge_kernel<T><<<g2, DEC_THREADS, 0, s>>>(P);
+    count_launch(2);
+    return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  }
+  const bool vec = P.d_h % 8 == 0;
+  if (P.d_vh <= 64) {
+    if (vec) decode_partial_kernel<T, 2, true><<<g1, DEC_THREADS, 0, s>>>(P);
+    else decode_partial_kernel<T, 2, false><<<g1, DEC_THREADS, 0, s>>>(P);
+  } else if (P.d_vh <= 128) {
+    if (vec) decode_partial_kernel<T, 4, true><<<g1, DEC_THREADS, 0, s>>>(P);
+    else decode_partial_kernel<T, 4, false><<<g1, DEC_THREADS, 0, s>>>(P);
+  } else {
+    if (vec) decode_partial_kernel<T, 8, true><<<g1, DEC_THREADS, 0, s>>>(P);
+    else decode_partial_kernel<T, 8, false><<<g1, DEC_THREADS, 0, s>>>(P);
+  }
+  decode_merge_kernel<T><<<g2, DEC_THREADS, 0, s>>>(P);
+  count_launch(2);
+  return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int B, int n_q, int n_k, int h, int d_vh) {
+  const size_t nsplit = (size_t)((n_k + DEC_CHUNK - 1) / DEC_CHUNK) * DEC_WARPS;
+  return (size_t)B * h * n_q * nsplit * (2 + (size_t)d_vh) * sizeof(float);
+}
+
+mha_status attention_decode(const DecodeArgs& a, mha_dtype dt, cudaStream_t s) {
+  if (a.d_h > 256 || a.d_vh > 256) return MHA_ERR_UNSUPPORTED;
+  const int nchunk = (a.n_k + DEC_CHUNK - 1) / DEC_CHUNK;
+  if (nchunk * DEC_WARPS > 1024) return MHA_ERR_UNSUPPORTED;  // merge weights in shared memory
+  if (a.h > 65535 || a.B > 65535) return MHA_ERR_UNSUPPORTED;
+  DecodeParams P;
+  P.Q = a.Q;
+  P.K = a.K;
+  P.V = a.V;
+  P.Z = a.Z;
+  P.part = static_cast<float*>(a.part);
+  P.B = a.B;
+  P.n_q = a.n_q;
+  P.n_k = a.n_k;
+  P.h = a.h;
+  P.d_h = a.d_h;
+  P.d_vh = a.d_vh;
+  P.nsplit = nchunk * DEC_WARPS;
+  P.cl2 = a.c * 1.4426950408889634f;
+  P.causal_tail = a.causal_tail;
+  for (int b = 0; b < MHA_MAX_PADDED_BATCH; ++b)
+    P.valid_len[b] = (a.cache_len_host && b < a.B) ? a.cache_len_host[b] : a.n_k;
+  if (dt == MHA_DTYPE_F32) return launch_decode<float>(P, nchunk, s);
+  return launch_decode<__nv_bfloat16>(P, nchunk, s);
+}
+
+}  // namespace mha

@@ -55,6 +55,24 @@ struct AttnArgs {
   int32_t* err;
 };
 
+// Attention of a few query rows over a key/value cache, split over the keys
+// (decode.cu). Q (B,h,n_q,d_h), K (B,h,n_k,d_h), V (B,h,n_k,d_vh) head-split;
+// Z (B,n_q,h*d_vh); part: decode_workspace_bytes of device scratch.
+struct DecodeArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* Z;
+  void* part;
+  int B, n_q, n_k, h, d_h, d_vh;
+  float c;
+  int causal_tail;                 // row i sees keys j <= L_b - n_q + i
+  const int32_t* cache_len_host;   // B entries, or null (every length n_k)
+};
+
+size_t decode_workspace_bytes(int B, int n_q, int n_k, int h, int d_vh);
+mha_status attention_decode(const DecodeArgs& a, mha_dtype dt, cudaStream_t s);
+
 // Kernel limit for bounded waits (nanoseconds).
 uint64_t wait_limit_ns();
 void count_launch(int n = 1);

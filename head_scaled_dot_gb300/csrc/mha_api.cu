@@ -382,6 +382,55 @@ mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q, const
                              stream);
 }
 
+size_t mha_decode_workspace_size(int B, int n_q, int n_k, int h, int d_vh) {
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_vh <= 0) return 0;
+  return decode_workspace_bytes(B, n_q, n_k, h, d_vh);
+}
+
+mha_status mha_attention_decode(const void* Q, const void* K, const void* V, void* Z, int B,
+                                int n_q, int n_k, int h, int d_h, int d_vh, float c,
+                                const int32_t* cache_len, int causal_tail, mha_dtype dt,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!Q || !K || !V || !Z) return MHA_ERR_INVALID_ARG;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
+    return MHA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt) || !isfinite(c)) return MHA_ERR_INVALID_ARG;
+  if (cache_len) {
+    if (B > MHA_MAX_PADDED_BATCH) return MHA_ERR_UNSUPPORTED;
+    for (int b = 0; b < B; ++b)
+      if (cache_len[b] < 1 || cache_len[b] > n_k || (causal_tail && cache_len[b] < n_q))
+        return MHA_ERR_EMPTY_ROW;
+  } else if (causal_tail && n_k < n_q) {
+    return MHA_ERR_EMPTY_ROW;
+  }
+  if (d_h > MAX_HEAD_DIM || d_vh > MAX_HEAD_DIM || n_k > 65536) return MHA_ERR_UNSUPPORTED;
+  if (!fits((long long)B * h, n_q, d_h) || !fits((long long)B * h, n_k, d_h) ||
+      !fits((long long)B * h, n_k, d_vh) || !fits((long long)B * h, n_q, d_vh))
+    return MHA_ERR_UNSUPPORTED;
+  if (dt == MHA_DTYPE_BF16 &&
+      (d_h % 8 || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Z)))
+    return MHA_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 15u) ||
+      workspace_bytes < decode_workspace_bytes(B, n_q, n_k, h, d_vh))
+    return MHA_ERR_WORKSPACE;
+  DecodeArgs a{};
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.Z = Z;
+  a.part = workspace;
+  a.B = B;
+  a.n_q = n_q;
+  a.n_k = n_k;
+  a.h = h;
+  a.d_h = d_h;
+  a.d_vh = d_vh;
+  a.c = c;
+  a.causal_tail = causal_tail ? 1 : 0;
+  a.cache_len_host = cache_len;
+  return attention_decode(a, dt, static_cast<cudaStream_t>(stream));
+}
+
 mha_status mha_get_device_error(void* error_word, void* stream) {
   if (!error_word) return MHA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -33,7 +33,8 @@ EXPORTS = (
     "mha_workspace_size", "mha_workspace_layout", "mha_forward", "mha_qkv_projection", "mha_attention",
     "mha_output_projection", "mha_get_device_error", "mha_status_string",
     "mha_selftest_wait_timeout", "mha_kernel_launch_count", "mha_version",
-    "mha_forward_no_alloc", "mha_forward_general",
+    "mha_forward_no_alloc", "mha_forward_general", "mha_decode_workspace_size",
+    "mha_attention_decode",
 )
 
 _lib = None
@@ -63,6 +64,10 @@ def load(path=LIB_PATH):
     lib.mha_forward.argtypes = [P] * 7 + [I] * 8 + [F, I, P, I, P, S, P]
     lib.mha_forward_general.restype = I
     lib.mha_forward_general.argtypes = [P] * 8 + [I] * 10 + [F, I, P, I, P, I, P, S, P]
+    lib.mha_decode_workspace_size.restype = S
+    lib.mha_decode_workspace_size.argtypes = [I] * 5
+    lib.mha_attention_decode.restype = I
+    lib.mha_attention_decode.argtypes = [P] * 4 + [I] * 6 + [F, P, I, I, P, S, P]
     lib.mha_forward_no_alloc.restype = I
     lib.mha_forward_no_alloc.argtypes = [P] * 7 + [I] * 8 + [F, I, P, I, P]
     lib.mha_qkv_projection.restype = I
@@ -270,6 +275,34 @@ def output_projection(Z, W_O, h, d_vh, out=None, dev_error=None, stream=None):
     st = lib.mha_output_projection(_ptr(Z), _ptr(W_O), _ptr(out), B, n_q, h, d_vh, d_o,
                                    DTYPES[dt], _ptr(dev_error), _stream(stream))
     _check(st, "mha_output_projection")
+    return out
+
+
+def decode_workspace_size(B, n_q, n_k, h, d_vh):
+    return int(load().mha_decode_workspace_size(B, n_q, n_k, h, d_vh))
+
+
+def attention_decode(Q, K, V, c, cache_len=None, causal_tail=False, out=None, workspace=None,
+                     stream=None):
+    """mha_attention_decode: Z (B, n_q, h*d_vh) for the new query rows Q
+    (B, h, n_q, d_h) over the cache K (B, h, n_k, d_h), V (B, h, n_k, d_vh)
+    holding cache_len[b] valid positions."""
+    lib = load()
+    B, h, n_q, d_h = Q.shape
+    n_k, d_vh = V.shape[2], V.shape[3]
+    dt = TORCH_DTYPES[Q.dtype]
+    if out is None:
+        out = torch.empty((B, n_q, h * d_vh), dtype=Q.dtype, device=Q.device)
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(B, n_q, n_k, h, d_vh), dtype=torch.uint8,
+                                device=Q.device)
+    lens, keep = _lens(cache_len, B)
+    st = lib.mha_attention_decode(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, n_q, n_k, h, d_h,
+                                  d_vh, float(c), lens, int(bool(causal_tail)), DTYPES[dt],
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    del keep
+    _check(st, "mha_attention_decode")
     return out
 
 

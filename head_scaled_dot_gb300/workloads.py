@@ -100,3 +100,44 @@ def make_inputs(w, lengths=None):
     }
     return out
 
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """New query rows over a key/value cache (head-split tensors)."""
+    name: str
+    B: int
+    h: int
+    n_q: int
+    n_k: int
+    d_h: int
+    d_vh: int
+    dtype: str
+    c: float
+    seed: int
+    causal_tail: bool = False
+
+
+# The decode workload of the benchmark: one new row per sequence over a cache
+# of capacity 8192, the sizes of the cross-attention workload's heads.
+DECODE = DecodeWorkload(name="decode_bf16_B16_h8_dh128_nq1_cache8192", B=16, h=8, n_q=1,
+                        n_k=8192, d_h=128, d_vh=128, dtype="bf16", c=1 / math.sqrt(128),
+                        seed=5)
+
+
+def make_decode_inputs(w, lengths=None):
+    """Draw Q (B, h, n_q, d_h), K (B, h, n_k, d_h), V (B, h, n_k, d_vh), each
+    N(0, 1), then one cache length per batch item, uniform on the integers
+    [ceil(n_k/2), n_k] (at least n_q with causal_tail); in this order, from one
+    torch CPU generator seeded with w.seed, rounded to the compute type."""
+    g = torch.Generator().manual_seed(int(w.seed))
+    Q = torch.randn((w.B, w.h, w.n_q, w.d_h), generator=g)
+    K = torch.randn((w.B, w.h, w.n_k, w.d_h), generator=g)
+    V = torch.randn((w.B, w.h, w.n_k, w.d_vh), generator=g)
+    lo = max(1, (w.n_k + 1) // 2, w.n_q if w.causal_tail else 1)
+    cache_len = torch.randint(lo, w.n_k + 1, (w.B,), generator=g).to(torch.int32)
+    if lengths is not None:
+        cache_len = torch.as_tensor(lengths, dtype=torch.int32).clone()
+    dt = torch_dtype(w.dtype)
+    return {"Q": Q.to(dt), "K": K.to(dt), "V": V.to(dt),
+            "cache_len": [int(x) for x in cache_len]}

@@ -229,6 +229,47 @@ MHA_API mha_status mha_output_projection(const void* Z, const void* W_O, void* Y
                                  mha_dtype dt, int32_t* dev_error,
                                  void* stream);
 
+/*
+ * Device scratch for mha_attention_decode, in bytes: one partial summary
+ * (m, l and d_vh values of z, fp32) per query row, head, batch item and
+ * split of the cache (one per 128 cache positions); 0 when an argument is
+ * non-positive.
+ */
+MHA_API size_t mha_decode_workspace_size(int B, int n_q, int n_k, int h, int d_vh);
+
+/*
+ * Attention of a few new query rows over a key/value cache: the workload of
+ * autoregressive generation named in "From Attention to Self-Attention
+ * review" (each new token attends to the cached positions), computed with the
+ * summary and merge of "Stable summary of an attention key block"
+ * (alphabetamath.cc, Definition): the cache is cut into splits, each split is
+ * summarised on its own, and the summaries are merged.
+ *
+ *   Q (B, h, n_q, d_h)    the new rows, head-split
+ *   K (B, h, n_k, d_h)    the cache, capacity n_k; batch item b holds
+ *   V (B, h, n_k, d_vh)   cache_len[b] valid positions 0 .. cache_len[b]-1
+ *   Z (B, n_q, h*d_vh)    output, concatenated layout (as mha_attention)
+ *   cache_len             HOST int32[B], each in [1, n_k]; NULL: all n_k
+ *   causal_tail           0: every row sees all cache_len[b] keys. 1: the n_q
+ *                         rows are the last positions of the sequence and row i
+ *                         sees keys j <= cache_len[b] - n_q + i (needs
+ *                         cache_len[b] >= n_q)
+ *   workspace             device scratch of mha_decode_workspace_size bytes,
+ *                         16-byte aligned, contents on entry irrelevant
+ *
+ * Errors (host checks before any launch): MHA_ERR_INVALID_ARG for NULL
+ * pointers, non-positive sizes, non-finite c; MHA_ERR_EMPTY_ROW for a cache
+ * length outside [1, n_k] (or below n_q with causal_tail);
+ * MHA_ERR_UNSUPPORTED for d_h or d_vh above 256, n_k above 65536, bf16 with
+ * d_h not a multiple of 8 or misaligned pointers; MHA_ERR_WORKSPACE for a
+ * missing or small workspace. Enqueues two kernels; asynchronous.
+ */
+MHA_API mha_status mha_attention_decode(const void* Q, const void* K, const void* V, void* Z,
+                                        int B, int n_q, int n_k, int h, int d_h, int d_vh,
+                                        float c, const int32_t* cache_len, int causal_tail,
+                                        mha_dtype dt, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
 /* Size of the device scratch built into the library for mha_forward_no_alloc. */
 #define MHA_NO_ALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -363,6 +363,39 @@ def mha_rows(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, mask, valid_len,
     return Z @ W_O, Z
 
 
+def decode_allowed(n_q, n_k, cache_len, causal_tail):
+    """Allowed key sets of n_q new query rows over a cache holding cache_len
+    positions ('From Attention to Self-Attention review': autoregressive
+    generation; a causal mask removes future positions, a padding mask the
+    positions that are not part of the sequence). Without causal_tail every
+    row sees keys 0 .. cache_len-1; with it the rows are the last n_q
+    positions of the sequence and row i sees keys j <= cache_len - n_q + i."""
+    allowed = np.zeros((n_q, n_k), dtype=bool)
+    for i in range(n_q):
+        last = cache_len - n_q + i if causal_tail else cache_len - 1
+        allowed[i, :last + 1] = True
+    return allowed
+
+
+def attention_decode(Q, K, V, c, cache_len=None, causal_tail=False):
+    """Z (B, n_q, h*d_vh) of head-split Q (B, h, n_q, d_h) over the cache K
+    (B, h, n_k, d_h), V (B, h, n_k, d_vh): each head by the dense definition
+    (attention), the heads concatenated in order."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, h, n_q, _ = Q.shape
+    n_k, d_vh = V.shape[2], V.shape[3]
+    Z = np.zeros((B, n_q, h * d_vh))
+    for b in range(B):
+        L = n_k if cache_len is None else int(cache_len[b])
+        if not 1 <= L <= n_k or (causal_tail and L < n_q):
+            raise EmptyAllowedRow("cache length %d" % L)
+        allowed = decode_allowed(n_q, n_k, L, causal_tail)
+        for i in range(h):
+            H, _ = attention(Q[b, i], K[b, i], V[b, i], c, allowed)
+            Z[b, :, i * d_vh:(i + 1) * d_vh] = H
+    return Z
+
+
 # ---------------------------------------------------------------------------
 # Work counts (the formulas the benchmark reports)
 # ---------------------------------------------------------------------------

@@ -160,3 +160,41 @@ def test_head_gates_must_be_finite_and_few_enough(lib):
     assert _gen(lib, gate=ctypes.cast(bad, ctypes.c_void_p)) == 1
     many = (ctypes.c_float * 1025)(*([1.0] * 1025))
     assert _gen(lib, gate=ctypes.cast(many, ctypes.c_void_p), h=1025, d_h=8, d_vh=8) == 2
+
+
+def _dec(lib, **kw):
+    """mha_attention_decode with fake pointers; every call here must be
+    rejected by the host checks."""
+    a = dict(Q=4096, K=8192, V=12288, Z=16384, B=2, n_q=3, n_k=100, h=2, d_h=64, d_vh=64,
+             c=0.125, lens=None, tail=0, dt=1, ws=1 << 20, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.mha_attention_decode(P(a["Q"]), P(a["K"]), P(a["V"]), P(a["Z"]), a["B"],
+                                    a["n_q"], a["n_k"], a["h"], a["d_h"], a["d_vh"], a["c"],
+                                    a["lens"], a["tail"], a["dt"], P(a["ws"]), a["ws_bytes"],
+                                    a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Q=None), 1), (dict(Z=None), 1), (dict(n_q=0), 1), (dict(d_vh=-1), 1),
+    (dict(c=math.inf), 1), (dict(dt=3), 1),
+    (dict(d_h=264), 2), (dict(n_k=70000), 2), (dict(d_h=36), 2), (dict(K=8200), 2),
+    (dict(ws=None), 4), (dict(ws=(1 << 20) + 8), 4), (dict(ws_bytes=64), 4),
+    (dict(n_k=2, tail=1), 3),                # tail rows need n_q <= cache length
+])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _dec(lib, **kw) == code
+
+
+def test_decode_rejects_cache_lengths_outside_the_cache(lib):
+    for v, tail in [((0, 50), 0), ((101, 50), 0), ((2, 50), 1)]:
+        lens, keep = _lens(*v)
+        assert _dec(lib, lens=lens, tail=tail) == 3
+
+
+def test_decode_workspace_size(lib):
+    from head_scaled_dot_gb300 import mha
+    assert mha.decode_workspace_size(0, 1, 1, 1, 1) == 0
+    a = mha.decode_workspace_size(2, 1, 1000, 4, 64)
+    assert a == mha.decode_workspace_size(2, 1, 1024, 4, 64) > 0
+    assert mha.decode_workspace_size(2, 3, 1000, 4, 64) == 3 * a

@@ -530,3 +530,43 @@ def test_head_gates_scale_each_heads_contribution_linearly():
     np.testing.assert_allclose(f([2.5, -1.0]), 2.5 * f([1.0, 0.0]) - f([0.0, 1.0]),
                                rtol=1e-12, atol=1e-14)
     assert np.all(f([0.0, 0.0]) == 0.0)
+
+
+# ---------------------------------------------------------------------------
+# New rows over a key/value cache (autoregressive generation)
+# ---------------------------------------------------------------------------
+
+def test_decode_allowed_sets_reduce_to_the_causal_and_padding_masks():
+    # the rows are the whole sequence: the tail-causal sets are the causal mask
+    for n in (1, 4, 9):
+        np.testing.assert_array_equal(O.decode_allowed(n, n, n, True),
+                                      O.allowed_keys(O.MASK_CAUSAL, n, n))
+    # the rows see the whole cache: the padding mask of the cache length
+    np.testing.assert_array_equal(O.decode_allowed(3, 10, 7, False),
+                                  O.allowed_keys(O.MASK_PADDING, 3, 10, 7))
+    # one new row: both readings agree (it is the last position)
+    np.testing.assert_array_equal(O.decode_allowed(1, 10, 7, True),
+                                  O.decode_allowed(1, 10, 7, False))
+    # tail rows: row i sees the first L - n_q + i + 1 keys
+    a = O.decode_allowed(3, 10, 6, True)
+    assert [int(r.sum()) for r in a] == [4, 5, 6]
+
+
+def test_decode_rows_equal_the_last_rows_of_causal_self_attention():
+    """The n_q newest rows over a cache equal the last n_q rows of causal
+    self-attention over the whole sequence."""
+    r = rng(190)
+    B, h, n, d = 2, 3, 11, 4
+    Q = r.standard_normal((B, h, n, d))
+    K = r.standard_normal((B, h, n, d))
+    V = r.standard_normal((B, h, n, d))
+    full = np.zeros((B, n, h * d))
+    for b in range(B):
+        for i in range(h):
+            H, _ = O.attention(Q[b, i], K[b, i], V[b, i], 0.6, O.allowed_keys(O.MASK_CAUSAL, n, n))
+            full[b, :, i * d:(i + 1) * d] = H
+    for n_q in (1, 3):
+        Z = O.attention_decode(Q[:, :, n - n_q:], K, V, 0.6, [n, n], causal_tail=True)
+        np.testing.assert_allclose(Z, full[:, n - n_q:], rtol=1e-13, atol=1e-15)
+    with pytest.raises(O.EmptyAllowedRow):
+        O.attention_decode(Q[:, :, :3], K, V, 0.6, [2, 5], causal_tail=True)
