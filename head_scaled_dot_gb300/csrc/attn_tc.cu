@@ -35,8 +35,24 @@
 //
 // Key blocks that are fully masked (past the causal diagonal, past the valid
 // length) are never loaded: they are the empty summary.
+//
+// Schedule. A unit is one tile pair of one (batch item, head). With no more
+// units than SMs every CTA takes one unit. Otherwise the host estimates two
+// schedules from the per-unit block counts (causal diagonal, valid lengths)
+// and launches the faster: one CTA per unit, handed out by the hardware in
+// order, or one persistent CTA per SM that walks a fixed list of units
+// (rounds of one unit per CTA, the CTA order reversed on odd rounds), with
+// the heavy causal pairs of every head first when K and V stay in L2. In a
+// persistent CTA the barrier phases run on from unit to unit: the next unit's
+// Q waits for the current unit's last S (q_empty), its first z = P V for the
+// epilogue to read the current z out (o_empty), and its K/V loads and first S
+// overlap the current unit's last blocks and epilogue.
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <algorithm>
+#include <functional>
+#include <vector>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -57,6 +73,10 @@ struct AttnTcParams {
   CUtensorMap vmap;  // V: dims {d_vh, n_k, B*h}, box {64, 128, 1}
   void* Z;
   int n_q, n_k, h;
+  int npair;         // 256-row query tile pairs per (batch item, head)
+  int units;         // npair * h * B
+  int nbh;           // h * B
+  int pi_major;      // units ordered by tile pair first (heavy causal pairs of every head first)
   float cl2;         // |c| * log2(e)
   int negate;        // c < 0: S is computed as -Q K^T (MMA negate-A bit)
   int causal, padding, pad_queries;
@@ -122,35 +142,54 @@ __device__ __forceinline__ int tile_blocks(const AttnTcParams& P, int tq0, int L
   return (k_end + BLK_N - 1) / BLK_N;
 }
 
+// One unit of work: the two 128-row query tiles starting at q0 of (b, head).
+struct Unit {
+  int q0, head, b, L, q_end;
+  int nb0, nb1, nmax;  // key blocks of tile 0, of tile 1, and the larger
+};
+
+// Units are numbered pair-fastest within each (batch item, head), or, with
+// pi_major, (batch item, head)-fastest within each tile pair; under a causal
+// mask the heavy pairs (large q0) come first either way.
+__host__ __device__ inline void unit_coords(int idx, int npair, int nbh, bool pi_major,
+                                            bool causal, int& pi, int& bh) {
+  pi = pi_major ? idx / nbh : idx % npair;
+  bh = pi_major ? idx % nbh : idx / npair;
+  if (causal) pi = npair - 1 - pi;
+}
+
+__device__ __forceinline__ Unit unit_at(const AttnTcParams& P, int idx) {
+  Unit u;
+  int pi, bh;
+  unit_coords(idx, P.npair, P.nbh, P.pi_major != 0, P.causal != 0, pi, bh);
+  u.head = bh % P.h;
+  u.b = bh / P.h;
+  u.q0 = pi * 2 * BLK_M;
+  u.L = P.padding ? P.valid_len[u.b] : P.n_k;
+  u.q_end = P.pad_queries ? min(u.L, P.n_q) : P.n_q;
+  u.nb0 = tile_blocks(P, u.q0, u.L, u.q_end);
+  u.nb1 = (u.q0 + BLK_M < P.n_q) ? tile_blocks(P, u.q0 + BLK_M, u.L, u.q_end) : 0;
+  u.nmax = u.nb1 > u.nb0 ? u.nb1 : u.nb0;  // tile 0's blocks are a prefix of tile 1's
+  return u;
+}
+
+// The i-th unit of this CTA, or -1 past the end. Round i hands units
+// [i G, i G + G) to the G CTAs, in reverse CTA order on odd rounds, so a CTA
+// that drew a heavy causal pair in one round draws a light one in the next.
+// With as many CTAs as units every CTA takes exactly its own unit.
+__device__ __forceinline__ int unit_index(const AttnTcParams& P, int i) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int idx = i * G + ((i & 1) ? G - 1 - c : c);
+  return idx < P.units ? idx : -1;
+}
+
 template <int DQK, int DV>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
   using C = ACfg<DQK, DV>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int npair = gridDim.x;
-  // causal: heavy tile pairs (large q0) first, so the light ones fill the tail
-  const int pi = P.causal ? (npair - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int q0 = pi * 2 * BLK_M;
-  const int head = blockIdx.y, b = blockIdx.z;
-  const int L = P.padding ? P.valid_len[b] : P.n_k;
-  const int q_end = P.pad_queries ? min(L, P.n_q) : P.n_q;
-  const int nb0 = tile_blocks(P, q0, L, q_end);
-  const int nb1 = (q0 + BLK_M < P.n_q) ? tile_blocks(P, q0 + BLK_M, L, q_end) : 0;
-  const int nmax = nb1 > nb0 ? nb1 : nb0;  // tile 0's blocks are a prefix of tile 1's
   __nv_bfloat16* Zg = static_cast<__nv_bfloat16*>(P.Z);
   const long long zrow_stride = (long long)P.h * DV;
-  const long long zbase = (long long)b * P.n_q * zrow_stride + (long long)head * DV;
-
-  if (nmax == 0) {
-    // every row of both tiles is padding: Z rows are exact zeros
-    const int r1 = min(q0 + 2 * BLK_M, P.n_q);
-    for (int e = threadIdx.x; e < (r1 - q0) * (DV / 8); e += NTHREADS) {
-      const int r = q0 + e / (DV / 8), c8 = e % (DV / 8);
-      *reinterpret_cast<uint4*>(Zg + zbase + (long long)r * zrow_stride + c8 * 8) =
-          make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -158,15 +197,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* q_s = smem;  // two Q tiles
   uint8_t* kv_s = smem + 2 * C::Q_TILE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + C::STAGES * C::STAGE_BYTES);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;            // [STAGES]
+  uint64_t* q_full = bars;                  // Q tiles of the current unit landed
+  uint64_t* q_empty = q_full + 1;           // both tiles' S of the unit done with Q
+  uint64_t* k_full = q_empty + 1;           // [STAGES]
   uint64_t* v_full = k_full + C::STAGES;    // [STAGES]
   uint64_t* k_empty = v_full + C::STAGES;   // [STAGES] freed once S of both tiles is done
   uint64_t* v_empty = k_empty + C::STAGES;  // [STAGES] freed once both z += P V are done
   uint64_t* s_full = v_empty + C::STAGES;   // [2] per tile
   uint64_t* p_full = s_full + 2;            // [2] per tile
   uint64_t* o_full = p_full + 2;            // [2] per tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 2);
+  uint64_t* o_empty = o_full + 2;           // [2] per tile: z read out by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   // partial row max / row sum exchange between partner softmax threads:
   // [2 halves][2 slots][128 rows] floats
@@ -174,16 +215,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 2);  // one arrival per MMA issuer
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], nb1 > 0 ? 2 : 1);  // one arrival per active tile
-      mbar_init(&v_empty[s], nb1 > 0 ? 2 : 1);
+      mbar_init(&k_empty[s], 2);  // one arrival per tile (issuer)
+      mbar_init(&v_empty[s], 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 8);  // one arrival per softmax warp
+      mbar_init(&p_full[t], 8);   // one arrival per softmax warp
       mbar_init(&o_full[t], 1);
+      mbar_init(&o_empty[t], 8);  // one arrival per softmax warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -197,13 +240,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{P.err, abort_flag, P.limit_ns};
-  const int bh = b * P.h + head;
 
   if (warp < 4) {
     if ((warp == 0 || warp == 2) && lane == 0) {
-      // warp 0 streams Q and the K blocks, warp 2 the V blocks; each also asks
-      // L2 for the blocks PREFETCH ahead so that refills of the ring come
-      // from L2 rather than DRAM
+      // warp 0 streams Q and the K blocks, warp 2 the V blocks, unit after
+      // unit through the same STAGES-deep ring (the ring position `it` runs
+      // on across units, so the next unit's first blocks load while the
+      // current unit's last ones are still being used); each also asks L2
+      // for the blocks PREFETCH ahead so that refills come from L2
       const bool is_k = warp == 0;
       const CUtensorMap* map = is_k ? &P.kmap : &P.vmap;
       uint64_t* full = is_k ? k_full : v_full;
@@ -211,37 +255,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int panels = is_k ? DQK / 64 : DV / 64;
       const uint32_t bytes = is_k ? C::K_BYTES : C::V_BYTES;
       tma_prefetch_desc(map);
-      if (is_k) {
-        tma_prefetch_desc(&P.qmap);
-        const int ntiles = nb1 > 0 ? 2 : 1;
-        mbar_arrive_expect_tx(q_full, ntiles * C::Q_TILE_BYTES);
-        for (int t = 0; t < ntiles; ++t)
-#pragma unroll
-          for (int p = 0; p < DQK / 64; ++p)
-            tma_load_3d(q_s + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, q_full, 64 * p,
-                        q0 + t * BLK_M, bh);
-      }
-      for (int kb = C::STAGES; kb < C::STAGES + PREFETCH && kb < nmax; ++kb)
-        for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, kb * BLK_N, bh);
-      int kb = 0;
+      if (is_k) tma_prefetch_desc(&P.qmap);
+      uint32_t it = 0;  // ring position
+      int ui = 0;       // units loaded so far
       bool gave_up = false;
-      for (; kb < nmax; ++kb) {
-        const int s = kb % C::STAGES;
-        uint8_t* dst = kv_s + s * C::STAGE_BYTES + (is_k ? 0 : C::K_BYTES);
-        if (kb >= C::STAGES && !mbar_wait(&empty[s], ((kb / C::STAGES) - 1) & 1, w)) {
-          gave_up = true;
-          break;
+      int q_last = -1;         // unit number of this thread's last Q load
+      for (int i = 0; !gave_up; ++i) {
+        const int idx = unit_index(P, i);
+        if (idx < 0) break;
+        const Unit u = unit_at(P, idx);
+        if (u.nmax == 0) continue;  // all rows padding: nothing to load
+        const int bh = u.b * P.h + u.head;
+        if (is_k) {
+          // the previous unit's S MMAs must be done reading the Q tiles
+          if (ui > 0 && !mbar_wait(q_empty, (ui - 1) & 1, w)) {
+            gave_up = true;
+            break;
+          }
+          const int ntiles = u.nb1 > 0 ? 2 : 1;
+          mbar_arrive_expect_tx(q_full, ntiles * C::Q_TILE_BYTES);
+          for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+            for (int p = 0; p < DQK / 64; ++p)
+              tma_load_3d(q_s + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, q_full, 64 * p,
+                          u.q0 + t * BLK_M, bh);
+          q_last = ui;
         }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        for (int p = 0; p < panels; ++p)
-          tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, kb * BLK_N, bh);
-        const int ahead = kb + C::STAGES + PREFETCH;
-        if (ahead < nmax)
-          for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, ahead * BLK_N, bh);
+        for (int kb = C::STAGES; kb < C::STAGES + PREFETCH && kb < u.nmax; ++kb)
+          for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, kb * BLK_N, bh);
+        for (int kb = 0; kb < u.nmax; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          uint8_t* dst = kv_s + s * C::STAGE_BYTES + (is_k ? 0 : C::K_BYTES);
+          if (it >= (uint32_t)C::STAGES &&
+              !mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, w)) {
+            gave_up = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          for (int p = 0; p < panels; ++p)
+            tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, kb * BLK_N, bh);
+          const int ahead = kb + C::STAGES + PREFETCH;
+          if (ahead < u.nmax)
+            for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, ahead * BLK_N, bh);
+        }
+        ++ui;
       }
       if (gave_up) {  // let this thread's loads land before the CTA exits
-        if (is_k) drain(q_full, 0);
-        for (int k = (kb > C::STAGES ? kb - C::STAGES : 0); k < kb; ++k)
+        if (is_k && q_last >= 0) drain(q_full, q_last & 1);
+        for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
           drain(&full[k % C::STAGES], (k / C::STAGES) & 1);
       }
     } else if ((warp == 1 || warp == 3) && lane == 0) {
@@ -249,9 +310,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Each keeps its own short tensor-instruction queue filled, so the
       // bookkeeping of one (barrier waits, commits) is covered by the other's
       // queued MMAs. Within a tile the order S_j, P_j V_j, S_{j+1}, ... is kept
-      // by the single issuing thread (S_{j+1} overwrites P_j in TMEM).
+      // by the single issuing thread (S_{j+1} overwrites P_j in TMEM); the
+      // next unit's first S follows the current unit's last P V the same way,
+      // so it runs while the softmax warps write the current unit out.
       const int t = warp == 1 ? 0 : 1;
-      const int nbt = t ? nb1 : nb0;
       const uint32_t idesc_qk =
           idesc_bf16_f32(BLK_M, BLK_N, 0, 0) | (P.negate ? (1u << 13) : 0u);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BLK_M, DV, 0, 1);
@@ -264,8 +326,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint64_t STAGE_D = C::STAGE_BYTES >> 4;
       const uint32_t s_tmem = tmem + (t ? C::S_COL1 : C::S_COL0);
       const uint32_t o_tmem = tmem + (t ? C::O_COL1 : C::O_COL0);
-      auto issue_s = [&](int kb) {
-        const uint64_t kd = k_desc + (uint64_t)(kb % C::STAGES) * STAGE_D;
+      // r: ring position of the K/V block
+      auto issue_s = [&](uint32_t r) {
+        const uint64_t kd = k_desc + (uint64_t)(r % C::STAGES) * STAGE_D;
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           // 16 elements = 32 B inside a 128 B swizzle row; 64-element panels 16 KB apart
@@ -273,59 +336,100 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           umma_ss(s_tmem, qd + off, kd + off, idesc_qk, kk > 0);
         }
         umma_commit(&s_full[t]);
-        umma_commit(&k_empty[kb % C::STAGES]);  // this tile is done with K_kb
+        umma_commit(&k_empty[r % C::STAGES]);  // this tile is done with this K block
       };
-      auto issue_pv = [&](int kb) {
-        const uint64_t vd = v_desc + (uint64_t)(kb % C::STAGES) * STAGE_D;
+      auto issue_pv = [&](uint32_t r, bool first) {
+        const uint64_t vd = v_desc + (uint64_t)(r % C::STAGES) * STAGE_D;
 #pragma unroll
         for (int kk = 0; kk < BLK_N / 16; ++kk) {
           // V is MN-major: 16 key rows of 128 B; 64-column panels 16 KB apart
           umma_ts(o_tmem, s_tmem + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc_pv,
-                  (kb > 0 || kk > 0));
+                  (!first || kk > 0));
         }
         umma_commit(&o_full[t]);
-        umma_commit(&v_empty[kb % C::STAGES]);  // this tile is done with V_kb
+        umma_commit(&v_empty[r % C::STAGES]);  // this tile is done with this V block
       };
-      bool ok = nbt > 0 && mbar_wait(q_full, 0, w);
-      int kb = 0;
-      if (ok && mbar_wait(&k_full[0], 0, w)) {
-        tc_fence_after();
-        issue_s(0);
-        for (; kb < nbt; ++kb) {
-          const int s = kb % C::STAGES;
-          if (!mbar_wait(&v_full[s], (kb / C::STAGES) & 1, w) ||
-              !mbar_wait(&p_full[t], kb & 1, w)) {
+      uint32_t base = 0;  // ring position of the current unit's block 0
+      uint32_t c = 0;     // blocks of this tile folded so far (s/p/o_full phases)
+      uint32_t act = 0;   // units in which this tile had rows to compute
+      int ui = 0;
+      bool ok = true;
+      bool inflight = false;  // MMAs of this thread may still be running
+      for (int i = 0; ok; ++i) {
+        const int idx = unit_index(P, i);
+        if (idx < 0) break;
+        const Unit u = unit_at(P, idx);
+        if (u.nmax == 0) continue;
+        const int nbt = t ? u.nb1 : u.nb0;
+        // the unit's Q tiles are in (this also orders the q_empty arrival
+        // below after the previous unit's phase)
+        if (!mbar_wait(q_full, ui & 1, w)) {
+          ok = false;
+          break;
+        }
+        if (nbt > 0) {
+          if (!mbar_wait(&k_full[base % C::STAGES], (base / C::STAGES) & 1, w)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(kb);
-          if (kb + 1 < nbt) {
-            if (!mbar_wait(&k_full[(kb + 1) % C::STAGES], ((kb + 1) / C::STAGES) & 1, w)) {
+          issue_s(base);
+          inflight = true;
+          if (nbt == 1) umma_commit(q_empty);  // the unit's last S is issued
+          for (int kb = 0; kb < nbt; ++kb, ++c) {
+            const uint32_t r = base + kb;
+            const int s = r % C::STAGES;
+            if (!mbar_wait(&v_full[s], (r / C::STAGES) & 1, w) ||
+                !mbar_wait(&p_full[t], c & 1, w)) {
+              ok = false;
+              break;
+            }
+            // the previous unit's z must have been read out before the first
+            // z = P V of this unit overwrites it
+            if (kb == 0 && act > 0 && !mbar_wait(&o_empty[t], (act - 1) & 1, w)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_s(kb + 1);  // after P_kb V_kb in this thread's order
+            issue_pv(r, kb == 0);
+            if (kb + 1 < nbt) {
+              if (!mbar_wait(&k_full[(r + 1) % C::STAGES], ((r + 1) / C::STAGES) & 1, w)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(r + 1);  // after P_kb V_kb in this thread's order
+              if (kb + 2 == nbt) umma_commit(q_empty);  // the unit's last S is issued
+            }
           }
+          if (!ok) break;
+          ++act;
+        } else {
+          mbar_arrive(q_empty);  // this tile has no rows in the unit: no S reads Q
         }
-      } else {
-        ok = nbt == 0;
-      }
-      // Causal tile 0 needs fewer blocks than tile 1; it still releases the
-      // remaining K/V stages, each once that block's data is in (so the
-      // arrival lands in that block's phase of the empty barrier).
-      if (ok && nbt > 0) {
-        for (int k2 = nbt; k2 < nmax; ++k2) {
-          const int s = k2 % C::STAGES;
-          const uint32_t par = (k2 / C::STAGES) & 1;
-          if (!mbar_wait(&k_full[s], par, w)) break;
+        // A tile with fewer blocks than the unit (causal tile 0, or a padding
+        // tile 1) still releases the remaining K/V stages, each once that
+        // block's data is in (so the arrival lands in that block's phase of
+        // the empty barrier).
+        for (int k2 = nbt; k2 < u.nmax && ok; ++k2) {
+          const uint32_t r = base + k2;
+          const int s = r % C::STAGES;
+          const uint32_t par = (r / C::STAGES) & 1;
+          if (!mbar_wait(&k_full[s], par, w)) {
+            ok = false;
+            break;
+          }
           mbar_arrive(&k_empty[s]);
-          if (!mbar_wait(&v_full[s], par, w)) break;
+          if (!mbar_wait(&v_full[s], par, w)) {
+            ok = false;
+            break;
+          }
           mbar_arrive(&v_empty[s]);
         }
+        base += u.nmax;
+        ++ui;
       }
-      if (!ok && nbt > 0) {  // gave up: wait for this thread's MMAs before TMEM is released
+      if (!ok && inflight) {  // gave up: wait for this thread's MMAs before TMEM is released
         umma_commit(&s_full[t]);
         drain(&s_full[t], 0);
         drain(&s_full[t], 1);
@@ -339,7 +443,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // selects key columns [64 half, 64 half + 64) of S and value columns
     // [half DV/2, (half + 1) DV/2) of z. The partners combine their partial
     // row max through shared memory (a 64-thread named barrier) and keep
-    // partial row sums, added once at the end.
+    // partial row sums, added once at the end of a unit.
     const int g = warp & 3;           // TMEM lane slice 32*g .. 32*g+31
     const int half = (warp - 4) >> 2;  // 0: warps 4..7, 1: warps 8..11
     const int r = 32 * g + lane;
@@ -351,157 +455,175 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto pair_sync = [&]() {
       asm volatile("bar.sync %0, 64;" ::"r"(1 + g) : "memory");
     };
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    int xc = 0;  // exchanges so far (alternates the shared slots)
+    uint32_t c[2] = {0, 0};  // blocks folded per tile so far (s/p/o_full phases)
+    int xc = 0;              // exchanges so far (alternates the shared slots)
     bool ok = true;
-    // Every (block, tile) step below runs exactly one pair barrier on both
-    // partners, whatever happened before (a partner that gave up on a wait
-    // still takes part), so the named barriers can never be left waiting.
-    for (int kb = 0; kb < nmax; ++kb) {
+    // Every (block, tile) step and every tile epilogue below runs exactly one
+    // pair barrier on both partners, whatever happened before (a partner that
+    // gave up on a wait still takes part), so the named barriers can never be
+    // left waiting.
+    for (int i = 0;; ++i) {
+      const int idx = unit_index(P, i);
+      if (idx < 0) break;
+      const Unit u = unit_at(P, idx);
+      const long long zbase = (long long)u.b * P.n_q * zrow_stride + (long long)u.head * DV;
+      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+      for (int kb = 0; kb < u.nmax; ++kb) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int nblk = t ? nb1 : nb0;
-        if (kb >= nblk) continue;  // uniform across the pair
-        const int tq0 = q0 + t * BLK_M;
-        const int q = tq0 + r;
-        const uint32_t s_addr = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
-        const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
-        if (ok && !mbar_wait(&s_full[t], kb & 1, w)) ok = false;
-        if (!ok) {  // keep the pair in step, do no work
-          pair_sync();
-          ++xc;
-          continue;
-        }
-        tc_fence_after();
-        const int k0 = kb * BLK_N;
-        const bool masked = (k0 + BLK_N > L) || (P.causal && k0 + BLK_N - 1 > tq0);
-        // allowed keys of this row in this block: k0 + c < lim
-        const int lim = (masked ? (P.causal ? min(L, q + 1) : L) - k0 : BLK_N) - 64 * half;
-        uint32_t sr[64];
-        tmem_ld32(s_addr + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(s_addr + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_wait_ld();
-        if (masked) {
-          // forbidden keys get s = -inf, hence weight 2^{-inf} = 0 exactly
-          // (the scale cl2 is positive, never 0); blocks without forbidden
-          // keys skip this branch
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
-        }
-        // combine with the partner's half of the row; after this barrier both
-        // halves of S are in registers, so P may overwrite its columns
-        xch[128 * (xc & 1) + r] = max64(sr);
-        pair_sync();
-        const float mx = fmaxf(xch[128 * (xc & 1) + r], pxch[128 * (xc & 1) + r]);
-        ++xc;
-        const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
-        // raise the running max only past the threshold (or on the first block)
-        const bool raise =
-            (m_run[t] == -INFINITY) ? true : (m_blk > m_run[t] + RESCALE_LOG2);
-        const float m_new = raise ? fmaxf(m_run[t], m_blk) : m_run[t];
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ex2_approx(m_run[t] - m_use);  // e^{m - m'}: 1 when m is kept
-        const float2 negm = make_float2(-m_use, -m_use);
-        float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
-        // p = 2^{c log2(e) s - m} as bf16 into this half's P columns
-        // [32 half, 32 half + 32) of S (two bf16 per column)
-#pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            float2 x0 = __ffma2_rn(
-                make_float2(__uint_as_float(sr[c + j]), __uint_as_float(sr[c + j + 1])), cl2x2,
-                negm);
-            float2 x1 = __ffma2_rn(
-                make_float2(__uint_as_float(sr[c + j + 2]), __uint_as_float(sr[c + j + 3])),
-                cl2x2, negm);
-            x0.x = ex2_approx(x0.x);
-            x0.y = ex2_approx(x0.y);
-            x1.x = ex2_approx(x1.x);
-            x1.y = ex2_approx(x1.y);
-            sum = __fadd2_rn(sum, x0);
-            sum_b = __fadd2_rn(sum_b, x1);
-            pk[j / 2] = pack_bf16x2(x0.x, x0.y);
-            pk[j / 2 + 1] = pack_bf16x2(x1.x, x1.y);
-          }
-          tmem_st16(s_addr + 32 * half + c / 2, pk);
-        }
-        l_run[t] = l_run[t] * alpha + ((sum.x + sum.y) + (sum_b.x + sum_b.y));
-        // merge: rescale this row of z by e^{m - m'} when m was raised; z must
-        // already hold every earlier block (wait for the previous z += P V)
-        if (__any_sync(0xffffffffu, kb > 0 && raise)) {
-          if (!mbar_wait(&o_full[t], (kb - 1) & 1, w)) {
+        for (int t = 0; t < 2; ++t) {
+          const int nblk = t ? u.nb1 : u.nb0;
+          if (kb >= nblk) continue;  // uniform across the pair
+          const int tq0 = u.q0 + t * BLK_M;
+          const int q = tq0 + r;
+          const uint32_t s_addr = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
+          const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
+          const uint32_t cc = c[t]++;
+          if (ok && !mbar_wait(&s_full[t], cc & 1, w)) ok = false;
+          if (!__all_sync(0xffffffffu, ok)) {  // keep the pair in step, do no work
             ok = false;
+            pair_sync();
+            ++xc;
             continue;
           }
           tc_fence_after();
+          const int k0 = kb * BLK_N;
+          const bool masked = (k0 + BLK_N > u.L) || (P.causal && k0 + BLK_N - 1 > tq0);
+          // allowed keys of this row in this block: k0 + c < lim
+          const int lim = (masked ? (P.causal ? min(u.L, q + 1) : u.L) - k0 : BLK_N) - 64 * half;
+          uint32_t sr[64];
+          tmem_ld32(s_addr + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          tmem_ld32(s_addr + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          tmem_wait_ld();
+          if (masked) {
+            // forbidden keys get s = -inf, hence weight 2^{-inf} = 0 exactly
+            // (the scale cl2 is positive, never 0); blocks without forbidden
+            // keys skip this branch
 #pragma unroll
-          for (int c = 0; c < DV / 64; ++c) {
-            uint32_t o[32];
-            const uint32_t oa = o_addr + half * (DV / 2) + 32 * c;
-            tmem_ld32(oa, o);
-            tmem_wait_ld();
+            for (int j = 0; j < 64; ++j)
+              if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
+          }
+          // combine with the partner's half of the row; after this barrier both
+          // halves of S are in registers, so P may overwrite its columns
+          xch[128 * (xc & 1) + r] = max64(sr);
+          pair_sync();
+          const float mx = fmaxf(xch[128 * (xc & 1) + r], pxch[128 * (xc & 1) + r]);
+          ++xc;
+          const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
+          // raise the running max only past the threshold (or on the first block)
+          const bool raise =
+              (m_run[t] == -INFINITY) ? true : (m_blk > m_run[t] + RESCALE_LOG2);
+          const float m_new = raise ? fmaxf(m_run[t], m_blk) : m_run[t];
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          const float alpha = ex2_approx(m_run[t] - m_use);  // e^{m - m'}: 1 when m is kept
+          const float2 negm = make_float2(-m_use, -m_use);
+          float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
+          // p = 2^{c log2(e) s - m} as bf16 into this half's P columns
+          // [32 half, 32 half + 32) of S (two bf16 per column)
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float2 v = __fmul2_rn(
-                  make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
-                  make_float2(alpha, alpha));
-              o[j] = __float_as_uint(v.x);
-              o[j + 1] = __float_as_uint(v.y);
+          for (int cb = 0; cb < 64; cb += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float2 x0 = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[cb + j]), __uint_as_float(sr[cb + j + 1])),
+                  cl2x2, negm);
+              float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[cb + j + 2]),
+                                                 __uint_as_float(sr[cb + j + 3])),
+                                     cl2x2, negm);
+              x0.x = ex2_approx(x0.x);
+              x0.y = ex2_approx(x0.y);
+              x1.x = ex2_approx(x1.x);
+              x1.y = ex2_approx(x1.y);
+              sum = __fadd2_rn(sum, x0);
+              sum_b = __fadd2_rn(sum_b, x1);
+              pk[j / 2] = pack_bf16x2(x0.x, x0.y);
+              pk[j / 2 + 1] = pack_bf16x2(x1.x, x1.y);
             }
-            tmem_st32(oa, o);
+            tmem_st16(s_addr + 32 * half + cb / 2, pk);
+          }
+          l_run[t] = l_run[t] * alpha + ((sum.x + sum.y) + (sum_b.x + sum_b.y));
+          // merge: rescale this row of z by e^{m - m'} when m was raised; z must
+          // already hold every earlier block (wait for the previous z += P V)
+          if (__any_sync(0xffffffffu, kb > 0 && raise)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&o_full[t], (cc - 1) & 1, w))) {
+              ok = false;
+              continue;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int cb = 0; cb < DV / 64; ++cb) {
+              uint32_t o[32];
+              const uint32_t oa = o_addr + half * (DV / 2) + 32 * cb;
+              tmem_ld32(oa, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                const float2 v = __fmul2_rn(
+                    make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
+                    make_float2(alpha, alpha));
+                o[j] = __float_as_uint(v.x);
+                o[j + 1] = __float_as_uint(v.y);
+              }
+              tmem_st32(oa, o);
+            }
+          }
+          m_run[t] = m_new;
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_full[t]);
+        }
+      }
+      // Epilogue of the unit: z / l for this half of each row, in the
+      // concatenated layout; then z of the tile is free for the next unit.
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int nblk = t ? u.nb1 : u.nb0;
+        const int q = u.q0 + t * BLK_M + r;
+        const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
+        __nv_bfloat16* zrow = Zg + zbase + (long long)q * zrow_stride + half * (DV / 2);
+        if (nblk == 0) {
+          // the whole tile is padding: its rows are zero
+          if (q < P.n_q) {
+#pragma unroll
+            for (int j = 0; j < DV / 16; ++j)
+              reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
+          }
+          continue;
+        }
+        // the row sum is the two partners' partial sums (same running max)
+        xch[128 * (xc & 1) + r] = l_run[t];
+        pair_sync();
+        const float l_tot = l_run[t] + pxch[128 * (xc & 1) + r];
+        ++xc;
+        if (!ok || !__all_sync(0xffffffffu, mbar_wait(&o_full[t], (c[t] - 1) & 1, w))) {
+          ok = false;
+          continue;
+        }
+        tc_fence_after();
+        const bool computed = q < u.q_end;
+        const float inv = computed ? P.head_gate[u.head] / l_tot : 0.f;
+#pragma unroll
+        for (int cb = 0; cb < DV / 64; ++cb) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + half * (DV / 2) + 32 * cb, o);
+          tmem_wait_ld();
+          if (q < P.n_q) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[j] = computed ? pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
+                                             __uint_as_float(o[2 * j + 1]) * inv)
+                               : 0u;
+            uint4* dst = reinterpret_cast<uint4*>(zrow + 32 * cb);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           }
         }
-        m_run[t] = m_new;
-        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[t]);
-      }
-    }
-    // Epilogue: z / l for this half of each row, in the concatenated layout.
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const int nblk = t ? nb1 : nb0;
-      const int q = q0 + t * BLK_M + r;
-      const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
-      __nv_bfloat16* zrow = Zg + zbase + (long long)q * zrow_stride + half * (DV / 2);
-      if (nblk == 0) {
-        // the whole tile is padding (tile 1 only): its rows are zero
-        if (q < P.n_q) {
-#pragma unroll
-          for (int j = 0; j < DV / 16; ++j) reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
-        }
-        continue;
-      }
-      // the row sum is the two partners' partial sums (same running max)
-      xch[128 * (xc & 1) + r] = l_run[t];
-      pair_sync();
-      const float l_tot = l_run[t] + pxch[128 * (xc & 1) + r];
-      ++xc;
-      if (!ok || !mbar_wait(&o_full[t], (nblk - 1) & 1, w)) continue;
-      tc_fence_after();
-      const bool computed = q < q_end;
-      const float inv = computed ? P.head_gate[head] / l_tot : 0.f;
-#pragma unroll
-      for (int c = 0; c < DV / 64; ++c) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + half * (DV / 2) + 32 * c, o);
-        tmem_wait_ld();
-        if (q < P.n_q) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = computed ? pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
-                                           __uint_as_float(o[2 * j + 1]) * inv)
-                             : 0u;
-          uint4* dst = reinterpret_cast<uint4*>(zrow + 32 * c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        }
+        if (lane == 0) mbar_arrive(&o_empty[t]);
       }
     }
   }
@@ -516,8 +638,86 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+// Host side of the schedule. The cost of a unit is counted in tile steps
+// (one 128 x 128 block of one tile); each CTA also pays a fixed part per unit
+// that it cannot overlap: in a CTA of its own, the start-up (loads, first S)
+// and the epilogue, about UNIT_FIXED steps on GB300; in a persistent CTA only
+// the epilogue, PERSIST_FIXED steps (the next unit's loads and first S run
+// under the current unit's last steps).
+constexpr int UNIT_FIXED = 5, PERSIST_FIXED = 2;
+constexpr long long MAX_SIMULATED_UNITS = 1 << 16;
+constexpr double PI_MAJOR_MAX_KV_BYTES = 96.0 * (1 << 20);  // K and V kept in L2
+
+int unit_steps_host(const AttnTcParams& P, int idx) {
+  int pi, bh;
+  unit_coords(idx, P.npair, P.nbh, P.pi_major != 0, P.causal != 0, pi, bh);
+  const int b = bh / P.h;
+  const int L = P.padding ? P.valid_len[b] : P.n_k;
+  const int q_end = P.pad_queries ? (L < P.n_q ? L : P.n_q) : P.n_q;
+  const int q0 = pi * 2 * BLK_M;
+  auto blocks = [&](int tq0) {
+    if (tq0 >= q_end) return 0;
+    int k_end = L;
+    if (P.causal && tq0 + BLK_M < k_end) k_end = tq0 + BLK_M;
+    return (k_end + BLK_N - 1) / BLK_N;
+  };
+  return blocks(q0) + (q0 + BLK_M < P.n_q ? blocks(q0 + BLK_M) : 0);
+}
+
+// Time of the static schedule of unit_index() on G persistent CTAs.
+long long persistent_makespan(const AttnTcParams& P, int G) {
+  long long worst = 0;
+  for (int c = 0; c < G; ++c) {
+    long long t = 0;
+    for (int i = 0;; ++i) {
+      const long long idx = (long long)i * G + ((i & 1) ? G - 1 - c : c);
+      if (idx >= P.units) break;
+      t += unit_steps_host(P, (int)idx) + PERSIST_FIXED;
+    }
+    worst = t > worst ? t : worst;
+  }
+  return worst;
+}
+
+// Time of one CTA per unit on G SMs: the hardware hands the units out in
+// order, each to the first SM that becomes free.
+long long per_unit_makespan(const AttnTcParams& P, int G) {
+  std::vector<long long> free_at((size_t)G, 0);
+  std::make_heap(free_at.begin(), free_at.end(), std::greater<long long>());
+  for (int idx = 0; idx < P.units; ++idx) {
+    std::pop_heap(free_at.begin(), free_at.end(), std::greater<long long>());
+    free_at.back() += unit_steps_host(P, idx) + UNIT_FIXED;
+    std::push_heap(free_at.begin(), free_at.end(), std::greater<long long>());
+  }
+  return *std::max_element(free_at.begin(), free_at.end());
+}
+
+// Picks one CTA per unit or a persistent grid (and the unit order) for the
+// shorter estimated time; returns the grid size.
+int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh) {
+  const int G = num_sms();
+  P.pi_major = 0;
+  if (P.units <= G) return P.units;
+  if (!P.causal && !P.padding) return G;  // equal units: the persistent grid only saves
+  if (P.units > MAX_SIMULATED_UNITS) return P.units;
+  const long long one_each = per_unit_makespan(P, G);
+  long long best = persistent_makespan(P, G);
+  int best_pi_major = 0;
+  const double kv_bytes = (double)B * P.h * P.n_k * (d_h + d_vh) * 2.0;
+  if (P.causal && kv_bytes <= PI_MAJOR_MAX_KV_BYTES) {
+    P.pi_major = 1;
+    const long long t = persistent_makespan(P, G);
+    if (t < best) {
+      best = t;
+      best_pi_major = 1;
+    }
+  }
+  P.pi_major = best < one_each ? best_pi_major : 0;
+  return best < one_each ? G : P.units;
+}
+
 template <int DQK, int DV>
-mha_status launch(const AttnTcParams& P, int B, int h, int n_q, cudaStream_t s) {
+mha_status launch(const AttnTcParams& P, int grid, cudaStream_t s) {
   using C = ACfg<DQK, DV>;
   static bool attr = false;
   if (!attr) {
@@ -526,7 +726,6 @@ mha_status launch(const AttnTcParams& P, int B, int h, int n_q, cudaStream_t s) 
       return MHA_ERR_CUDA;
     attr = true;
   }
-  const dim3 grid((n_q + 2 * BLK_M - 1) / (2 * BLK_M), h, B);
   attn_tc_kernel<DQK, DV><<<grid, NTHREADS, C::SMEM, s>>>(P);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
@@ -535,7 +734,6 @@ mha_status launch(const AttnTcParams& P, int B, int h, int n_q, cudaStream_t s) 
 }  // namespace
 
 mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
-  if (a.h > 65535 || a.B > 65535) return MHA_ERR_UNSUPPORTED;
   AttnTcParams P;
   memset(&P, 0, sizeof(P));
   const uint64_t BH = (uint64_t)a.B * a.h;
@@ -554,6 +752,11 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
   P.n_q = a.n_q;
   P.n_k = a.n_k;
   P.h = a.h;
+  P.npair = (a.n_q + 2 * BLK_M - 1) / (2 * BLK_M);
+  const long long units = (long long)P.npair * a.h * a.B;
+  if (units > (1ll << 30)) return MHA_ERR_UNSUPPORTED;
+  P.units = (int)units;
+  P.nbh = a.h * a.B;
   // |c| log2(e), kept at 1e-30 or above so that a masked score (-inf) stays
   // -inf after scaling; for c = 0 (or |c| below that) every allowed score
   // scales to within 1e-26 of 0 and gets weight 2^0 = 1: the uniform
@@ -569,10 +772,12 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
     P.valid_len[b] = (a.padding && b < a.B) ? a.valid_len_host[b] : a.n_k;
   for (int i = 0; i < MHA_MAX_GATED_HEADS; ++i)
     P.head_gate[i] = (a.head_gate_host && i < a.h) ? a.head_gate_host[i] : 1.f;
-  if (a.d_h == 64 && a.d_vh == 64) return launch<64, 64>(P, a.B, a.h, a.n_q, s);
-  if (a.d_h == 128 && a.d_vh == 128) return launch<128, 128>(P, a.B, a.h, a.n_q, s);
-  if (a.d_h == 64 && a.d_vh == 128) return launch<64, 128>(P, a.B, a.h, a.n_q, s);
-  if (a.d_h == 128 && a.d_vh == 64) return launch<128, 64>(P, a.B, a.h, a.n_q, s);
+  // one CTA per unit, or one persistent CTA per SM walking its share
+  const int grid = choose_schedule(P, a.B, a.d_h, a.d_vh);
+  if (a.d_h == 64 && a.d_vh == 64) return launch<64, 64>(P, grid, s);
+  if (a.d_h == 128 && a.d_vh == 128) return launch<128, 128>(P, grid, s);
+  if (a.d_h == 64 && a.d_vh == 128) return launch<64, 128>(P, grid, s);
+  if (a.d_h == 128 && a.d_vh == 64) return launch<128, 64>(P, grid, s);
   return MHA_ERR_UNSUPPORTED;
 }
 

@@ -173,6 +173,43 @@ def test_attention_step_alone(d, mask):
     assert rel_err(got, ref) <= 1e-2
 
 
+@pytest.mark.parametrize("d", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("mask", ["none", "causal", "padding", "causal_padding"])
+def test_attention_more_units_than_sms(d, mask):
+    """More tile pairs than SMs, so that CTAs take several units in turn: the
+    barrier phases carried from unit to unit, tiles with no rows (valid length
+    at most 128 into the pair) and pairs that are all padding."""
+    d_h, d_vh = d
+    B, h, n = 24, 4, 700  # 3 tile pairs per (batch item, head): 288 units
+    g = torch.Generator().manual_seed(7 * d_h + len(mask))
+    Q = torch.randn((B, h, n, d_h), generator=g).bfloat16()
+    K = torch.randn((B, h, n, d_h), generator=g).bfloat16()
+    V = torch.randn((B, h, n, d_vh), generator=g).bfloat16()
+    lens = None
+    if "padding" in mask:
+        lens = [700, 1, 128, 129, 255, 256, 257, 300, 511, 512, 513, 699] * 2
+    c = 1 / math.sqrt(d_h)
+    Z = mha.attention(Q.cuda(), K.cuda(), V.cuda(), c, mask, lens, self_attention=True)
+    torch.cuda.synchronize()
+    got = f64(Z)
+    ref = np.zeros((B, n, h * d_vh))
+    for b in range(B):
+        L = None if lens is None else lens[b]
+        rows = oracle.query_rows_computed(oracle.MASK_NAMES[mask], n, L, True)
+        allowed = oracle.allowed_keys(oracle.MASK_NAMES[mask], n, n, L)
+        for i in range(h):
+            H, _ = oracle.attention(f64(Q[b, i]), f64(K[b, i]), f64(V[b, i]), c, allowed, rows)
+            ref[b, :, i * d_vh:(i + 1) * d_vh] = H
+        if L is not None:
+            assert np.all(got[b, L:] == 0.0), "padded query rows must be exactly zero"
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref) <= 1e-2
+    # a second call on the same buffers gives the same bits
+    Z2 = mha.attention(Q.cuda(), K.cuda(), V.cuda(), c, mask, lens, self_attention=True)
+    torch.cuda.synchronize()
+    assert torch.equal(Z.cpu(), Z2.cpu())
+
+
 # ---------------------------------------------------------------------------
 # Statements of the pages checked on the GPU
 # ---------------------------------------------------------------------------
