@@ -74,7 +74,9 @@ struct AttnTcParams {
   void* Z;
   int n_q, n_k, h;
   int npair;         // 256-row query tile pairs per (batch item, head)
-  int units;         // npair * h * B
+  int units;         // units of work: pair_units pairs, then single tiles
+  int pair_units;    // the first pair_units units are tile pairs; each later
+                     // pair of the order is split into two single-tile units
   int nbh;           // h * B
   int pi_major;      // units ordered by tile pair first (heavy causal pairs of every head first)
   float cl2;         // |c| * log2(e)
@@ -142,33 +144,46 @@ __device__ __forceinline__ int tile_blocks(const AttnTcParams& P, int tq0, int L
   return (k_end + BLK_N - 1) / BLK_N;
 }
 
-// One unit of work: the two 128-row query tiles starting at q0 of (b, head).
+// One unit of work: the 128-row query tile starting at q0 of (b, head) and,
+// for a pair unit, the tile after it.
 struct Unit {
   int q0, head, b, L, q_end;
   int nb0, nb1, nmax;  // key blocks of tile 0, of tile 1, and the larger
+  bool pair;           // tile 1 belongs to this unit (its rows are written here)
 };
 
-// Units are numbered pair-fastest within each (batch item, head), or, with
-// pi_major, (batch item, head)-fastest within each tile pair; under a causal
-// mask the heavy pairs (large q0) come first either way.
-__host__ __device__ inline void unit_coords(int idx, int npair, int nbh, bool pi_major,
-                                            bool causal, int& pi, int& bh) {
-  pi = pi_major ? idx / nbh : idx % npair;
-  bh = pi_major ? idx % nbh : idx / npair;
-  if (causal) pi = npair - 1 - pi;
+// Tile pairs are ordered pair-fastest within each (batch item, head), or,
+// with pi_major, (batch item, head)-fastest within each pair index; under a
+// causal mask the heavy pairs (large q0) come first either way. Unit idx is
+// pair idx while idx < pair_units; after that, units pair_units + 2 j and
+// pair_units + 2 j + 1 are the two tiles of pair pair_units + j, on their own.
+__host__ __device__ inline void unit_coords(const AttnTcParams& P, int idx, int& pi, int& bh,
+                                            int& tile, bool& pair) {
+  int pidx = idx;
+  tile = 0;
+  pair = true;
+  if (idx >= P.pair_units) {
+    const int j = idx - P.pair_units;
+    pidx = P.pair_units + j / 2;
+    tile = j & 1;
+    pair = false;
+  }
+  pi = P.pi_major ? pidx / P.nbh : pidx % P.npair;
+  bh = P.pi_major ? pidx % P.nbh : pidx / P.npair;
+  if (P.causal) pi = P.npair - 1 - pi;
 }
 
 __device__ __forceinline__ Unit unit_at(const AttnTcParams& P, int idx) {
   Unit u;
-  int pi, bh;
-  unit_coords(idx, P.npair, P.nbh, P.pi_major != 0, P.causal != 0, pi, bh);
+  int pi, bh, tile;
+  unit_coords(P, idx, pi, bh, tile, u.pair);
   u.head = bh % P.h;
   u.b = bh / P.h;
-  u.q0 = pi * 2 * BLK_M;
+  u.q0 = pi * 2 * BLK_M + tile * BLK_M;
   u.L = P.padding ? P.valid_len[u.b] : P.n_k;
   u.q_end = P.pad_queries ? min(u.L, P.n_q) : P.n_q;
   u.nb0 = tile_blocks(P, u.q0, u.L, u.q_end);
-  u.nb1 = (u.q0 + BLK_M < P.n_q) ? tile_blocks(P, u.q0 + BLK_M, u.L, u.q_end) : 0;
+  u.nb1 = (u.pair && u.q0 + BLK_M < P.n_q) ? tile_blocks(P, u.q0 + BLK_M, u.L, u.q_end) : 0;
   u.nmax = u.nb1 > u.nb0 ? u.nb1 : u.nb0;  // tile 0's blocks are a prefix of tile 1's
   return u;
 }
@@ -578,6 +593,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // concatenated layout; then z of the tile is free for the next unit.
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
+        if (t == 1 && !u.pair) continue;  // those rows are another unit's
         const int nblk = t ? u.nb1 : u.nb0;
         const int q = u.q0 + t * BLK_M + r;
         const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
@@ -648,31 +664,35 @@ constexpr int UNIT_FIXED = 5, PERSIST_FIXED = 2;
 constexpr long long MAX_SIMULATED_UNITS = 1 << 16;
 constexpr double PI_MAJOR_MAX_KV_BYTES = 96.0 * (1 << 20);  // K and V kept in L2
 
-int unit_steps_host(const AttnTcParams& P, int idx) {
-  int pi, bh;
-  unit_coords(idx, P.npair, P.nbh, P.pi_major != 0, P.causal != 0, pi, bh);
+// A tile on its own cannot overlap its softmax with its MMAs: a step costs
+// the softmax plus the MMAs, about 1 + 4 (d_h + d_vh) / 1600 pair steps.
+double unit_cost_host(const AttnTcParams& P, int idx, double single_ratio) {
+  int pi, bh, tile;
+  bool pair;
+  unit_coords(P, idx, pi, bh, tile, pair);
   const int b = bh / P.h;
   const int L = P.padding ? P.valid_len[b] : P.n_k;
   const int q_end = P.pad_queries ? (L < P.n_q ? L : P.n_q) : P.n_q;
-  const int q0 = pi * 2 * BLK_M;
+  const int q0 = pi * 2 * BLK_M + tile * BLK_M;
   auto blocks = [&](int tq0) {
     if (tq0 >= q_end) return 0;
     int k_end = L;
     if (P.causal && tq0 + BLK_M < k_end) k_end = tq0 + BLK_M;
     return (k_end + BLK_N - 1) / BLK_N;
   };
+  if (!pair) return blocks(q0) * single_ratio;
   return blocks(q0) + (q0 + BLK_M < P.n_q ? blocks(q0 + BLK_M) : 0);
 }
 
 // Time of the static schedule of unit_index() on G persistent CTAs.
-long long persistent_makespan(const AttnTcParams& P, int G) {
-  long long worst = 0;
+double persistent_makespan(const AttnTcParams& P, int G, double sr) {
+  double worst = 0;
   for (int c = 0; c < G; ++c) {
-    long long t = 0;
+    double t = 0;
     for (int i = 0;; ++i) {
       const long long idx = (long long)i * G + ((i & 1) ? G - 1 - c : c);
       if (idx >= P.units) break;
-      t += unit_steps_host(P, (int)idx) + PERSIST_FIXED;
+      t += unit_cost_host(P, (int)idx, sr) + PERSIST_FIXED;
     }
     worst = t > worst ? t : worst;
   }
@@ -681,13 +701,13 @@ long long persistent_makespan(const AttnTcParams& P, int G) {
 
 // Time of one CTA per unit on G SMs: the hardware hands the units out in
 // order, each to the first SM that becomes free.
-long long per_unit_makespan(const AttnTcParams& P, int G) {
-  std::vector<long long> free_at((size_t)G, 0);
-  std::make_heap(free_at.begin(), free_at.end(), std::greater<long long>());
+double per_unit_makespan(const AttnTcParams& P, int G, double sr) {
+  std::vector<double> free_at((size_t)G, 0.0);
+  std::make_heap(free_at.begin(), free_at.end(), std::greater<double>());
   for (int idx = 0; idx < P.units; ++idx) {
-    std::pop_heap(free_at.begin(), free_at.end(), std::greater<long long>());
-    free_at.back() += unit_steps_host(P, idx) + UNIT_FIXED;
-    std::push_heap(free_at.begin(), free_at.end(), std::greater<long long>());
+    std::pop_heap(free_at.begin(), free_at.end(), std::greater<double>());
+    free_at.back() += unit_cost_host(P, idx, sr) + UNIT_FIXED;
+    std::push_heap(free_at.begin(), free_at.end(), std::greater<double>());
   }
   return *std::max_element(free_at.begin(), free_at.end());
 }
@@ -696,17 +716,34 @@ long long per_unit_makespan(const AttnTcParams& P, int G) {
 // shorter estimated time; returns the grid size.
 int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh) {
   const int G = num_sms();
+  const int pairs = P.npair * P.nbh;
+  const double sr = 1.0 + 4.0 * (d_h + d_vh) / 1600.0;
   P.pi_major = 0;
-  if (P.units <= G) return P.units;
-  if (!P.causal && !P.padding) return G;  // equal units: the persistent grid only saves
-  if (P.units > MAX_SIMULATED_UNITS) return P.units;
-  const long long one_each = per_unit_makespan(P, G);
-  long long best = persistent_makespan(P, G);
+  P.pair_units = P.units = pairs;
+  if (pairs <= G) return pairs;
+  if (!P.causal && !P.padding) {
+    // equal pairs: a persistent grid; the r pairs of a last, partly filled
+    // round become 2 r single tiles when that shortens it
+    const int r = pairs % G;
+    if (r > 0 && 2 * r <= G && pairs <= MAX_SIMULATED_UNITS) {
+      AttnTcParams S = P;
+      S.pair_units = pairs - r;
+      S.units = pairs + r;
+      if (persistent_makespan(S, G, sr) < persistent_makespan(P, G, sr)) {
+        P.pair_units = S.pair_units;
+        P.units = S.units;
+      }
+    }
+    return G;
+  }
+  if (pairs > MAX_SIMULATED_UNITS) return pairs;
+  const double one_each = per_unit_makespan(P, G, sr);
+  double best = persistent_makespan(P, G, sr);
   int best_pi_major = 0;
   const double kv_bytes = (double)B * P.h * P.n_k * (d_h + d_vh) * 2.0;
   if (P.causal && kv_bytes <= PI_MAJOR_MAX_KV_BYTES) {
     P.pi_major = 1;
-    const long long t = persistent_makespan(P, G);
+    const double t = persistent_makespan(P, G, sr);
     if (t < best) {
       best = t;
       best_pi_major = 1;
@@ -754,8 +791,8 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
   P.h = a.h;
   P.npair = (a.n_q + 2 * BLK_M - 1) / (2 * BLK_M);
   const long long units = (long long)P.npair * a.h * a.B;
-  if (units > (1ll << 30)) return MHA_ERR_UNSUPPORTED;
-  P.units = (int)units;
+  if (units > (1ll << 29)) return MHA_ERR_UNSUPPORTED;
+  P.units = P.pair_units = (int)units;
   P.nbh = a.h * a.B;
   // |c| log2(e), kept at 1e-30 or above so that a masked score (-inf) stays
   // -inf after scaling; for c = 0 (or |c| below that) every allowed score

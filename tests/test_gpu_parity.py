@@ -210,6 +210,33 @@ def test_attention_more_units_than_sms(d, mask):
     assert torch.equal(Z.cpu(), Z2.cpu())
 
 
+@pytest.mark.parametrize("d", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("n", [600, 640])
+def test_attention_last_round_split_into_single_tiles(d, n):
+    """198 tile pairs without a mask on a GPU of 152 SMs: the 46 pairs of the
+    last, partly filled round run as 92 single-tile units (n = 600: the second
+    tile of each last pair has no rows at all)."""
+    d_h, d_vh = d
+    B, h = 22, 3
+    g = torch.Generator().manual_seed(n + d_h)
+    Q = torch.randn((B, h, n, d_h), generator=g).bfloat16()
+    K = torch.randn((B, h, n, d_h), generator=g).bfloat16()
+    V = torch.randn((B, h, n, d_vh), generator=g).bfloat16()
+    c = 1 / math.sqrt(d_h)
+    Z = torch.full((B, n, h * d_vh), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mha.attention(Q.cuda(), K.cuda(), V.cuda(), c, "none", None, self_attention=True, out=Z)
+    torch.cuda.synchronize()
+    got = f64(Z)
+    ref = np.zeros((B, n, h * d_vh))
+    allowed = oracle.allowed_keys(oracle.MASK_NAMES["none"], n, n, None)
+    for b in range(B):
+        for i in range(h):
+            H, _ = oracle.attention(f64(Q[b, i]), f64(K[b, i]), f64(V[b, i]), c, allowed)
+            ref[b, :, i * d_vh:(i + 1) * d_vh] = H
+    assert np.isfinite(got).all(), "every row written exactly once"
+    assert rel_err(got, ref) <= 1e-2
+
+
 # ---------------------------------------------------------------------------
 # Statements of the pages checked on the GPU
 # ---------------------------------------------------------------------------
