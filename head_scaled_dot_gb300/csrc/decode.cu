@@ -280,16 +280,55 @@ __device__ __forceinline__ void load_cols(const T* p, float (&v)[CPL]) {
   }
 }
 
+// W consecutive 32-bit words at a 4 W-byte aligned address, in one load.
+template <int W>
+__device__ __forceinline__ void load_words(const void* p, uint32_t (&w)[W]) {
+  static_assert(W == 1 || W == 2 || W == 4, "words per load");
+  if constexpr (W == 1) {
+    w[0] = __ldg(reinterpret_cast<const unsigned int*>(p));
+  } else if constexpr (W == 2) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    w[0] = u.x;
+    w[1] = u.y;
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    w[0] = u.x;
+    w[1] = u.y;
+    w[2] = u.z;
+    w[3] = u.w;
+  }
+}
+
+// The CPL values held in the raw words of one load_words.
+template <typename T, int CPL, int W>
+__device__ __forceinline__ void unpack_words(const uint32_t (&w)[W], float (&v)[CPL]) {
+  if constexpr (sizeof(T) == 2) {
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] = __uint_as_float(w[i]);
+  }
+}
+
 // Pass 1 for head sizes known at compile time (d_h = DQK, d_vh = DV, both
 // multiples of 32 and of 8 elements per 16 bytes), NQ query rows per pass.
 // A lane issues every load of its key row before using any of them, and the
 // value rows are read as warp-wide vectors (lane owns columns
-// [lane*DV/32, (lane+1)*DV/32)), so many bytes are in flight per warp.
+// [lane*DV/32, (lane+1)*DV/32)); for a full group of 32 keys the value rows
+// are requested together with the key rows, before any arithmetic, so the
+// whole group (32 K rows and 32 V rows) is in flight per warp at once.
 template <typename T, int NQ, int DQK, int DV>
 __global__ void __launch_bounds__(DEC_THREADS) decode_partial_fast_kernel(
     const __grid_constant__ DecodeParams P) {
   constexpr int CPL = DV / 32;           // z columns per lane
   constexpr int KV16 = DQK / Vec16<T>::N; // 16-byte chunks per key row
+  constexpr int VW = CPL * (int)sizeof(T) / 4;  // 32-bit words of a lane's share of a V row
+  // value rows requested with the key rows when both fit in registers
+  constexpr bool V_AHEAD = 32 * VW + 4 * KV16 <= 128;
   __shared__ __align__(16) float qs[NQ][DQK];
   const int chunk = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -322,14 +361,23 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_partial_fast_kernel(
     for (int g0 = k0 + 32 * warp; g0 < k1; g0 += 32 * DEC_WARPS) {
       const int key = g0 + lane;
       const bool in = key < k1;
+      const bool full = V_AHEAD && g0 + 32 <= k1;  // uniform across the warp
+      const T* vbase = Vg + (long long)g0 * DV + lane * CPL;
       float s[NQ];
 #pragma unroll
       for (int r = 0; r < NQ; ++r) s[r] = 0.f;
+      uint32_t vraw[V_AHEAD ? 32 : 1][VW];
       if (in) {
         const uint4* krow = reinterpret_cast<const uint4*>(Kg + (long long)key * DQK);
         uint4 raw[KV16];
 #pragma unroll
         for (int i = 0; i < KV16; ++i) raw[i] = __ldg(krow + i);
+        if constexpr (V_AHEAD) {
+          if (full) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) load_words<VW>(vbase + (long long)j * DV, vraw[j]);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < KV16; ++i) {
           float kv[Vec16<T>::N];
@@ -360,17 +408,30 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_partial_fast_kernel(
         for (int t = 0; t < CPL; ++t) z_run[r][t] *= a;
         m_run[r] = m_new;
       }
-      const int ng = min(32, k1 - g0);
-      const T* vbase = Vg + (long long)g0 * DV + lane * CPL;
+      if (full) {
+#pragma unroll
+        for (int j = 0; j < (V_AHEAD ? 32 : 0); ++j) {
+          float vv[CPL];
+          unpack_words<T, CPL, VW>(vraw[j], vv);
+#pragma unroll
+          for (int r = 0; r < NQ; ++r) {
+            const float pj = __shfl_sync(0xffffffffu, p[r], j);
+#pragma unroll
+            for (int t = 0; t < CPL; ++t) z_run[r][t] = fmaf(pj, vv[t], z_run[r][t]);
+          }
+        }
+      } else {
+        const int ng = k1 - g0;
 #pragma unroll DEC_VUNROLL
-      for (int j = 0; j < ng; ++j) {
-        float vv[CPL];
-        load_cols<T, CPL>(vbase + (long long)j * DV, vv);
+        for (int j = 0; j < ng; ++j) {
+          float vv[CPL];
+          load_cols<T, CPL>(vbase + (long long)j * DV, vv);
 #pragma unroll
-        for (int r = 0; r < NQ; ++r) {
-          const float pj = __shfl_sync(0xffffffffu, p[r], j);
+          for (int r = 0; r < NQ; ++r) {
+            const float pj = __shfl_sync(0xffffffffu, p[r], j);
 #pragma unroll
-          for (int t = 0; t < CPL; ++t) z_run[r][t] = fmaf(pj, vv[t], z_run[r][t]);
+            for (int t = 0; t < CPL; ++t) z_run[r][t] = fmaf(pj, vv[t], z_run[r][t]);
+          }
         }
       }
     }
