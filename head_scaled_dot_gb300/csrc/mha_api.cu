@@ -395,8 +395,9 @@ mha_status mha_attention_decode(const void* Q, const void* K, const void* V, voi
   if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
     return MHA_ERR_INVALID_ARG;
   if (!dtype_ok(dt) || !isfinite(c)) return MHA_ERR_INVALID_ARG;
+  // the kernels take the cache lengths as a fixed-size launch argument
+  if (B > MHA_MAX_PADDED_BATCH) return MHA_ERR_UNSUPPORTED;
   if (cache_len) {
-    if (B > MHA_MAX_PADDED_BATCH) return MHA_ERR_UNSUPPORTED;
     for (int b = 0; b < B; ++b)
       if (cache_len[b] < 1 || cache_len[b] > n_k || (causal_tail && cache_len[b] < n_q))
         return MHA_ERR_EMPTY_ROW;

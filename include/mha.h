@@ -260,9 +260,10 @@ MHA_API size_t mha_decode_workspace_size(int B, int n_q, int n_k, int h, int d_v
  * Errors (host checks before any launch): MHA_ERR_INVALID_ARG for NULL
  * pointers, non-positive sizes, non-finite c; MHA_ERR_EMPTY_ROW for a cache
  * length outside [1, n_k] (or below n_q with causal_tail);
- * MHA_ERR_UNSUPPORTED for d_h or d_vh above 256, n_k above 65536, bf16 with
- * d_h not a multiple of 8 or misaligned pointers; MHA_ERR_WORKSPACE for a
- * missing or small workspace. Enqueues two kernels; asynchronous.
+ * MHA_ERR_UNSUPPORTED for B above MHA_MAX_PADDED_BATCH, d_h or d_vh above
+ * 256, n_k above 65536, bf16 with d_h not a multiple of 8 or misaligned
+ * pointers; MHA_ERR_WORKSPACE for a missing or small workspace. Enqueues two
+ * kernels; asynchronous.
  */
 MHA_API mha_status mha_attention_decode(const void* Q, const void* K, const void* V, void* Z,
                                         int B, int n_q, int n_k, int h, int d_h, int d_vh,

@@ -192,6 +192,15 @@ def test_decode_rejects_cache_lengths_outside_the_cache(lib):
         assert _dec(lib, lens=lens, tail=tail) == 3
 
 
+def test_decode_rejects_batches_beyond_the_length_table(lib):
+    """With or without cache lengths, a batch larger than the kernels' table
+    of per-item lengths is refused on the host, before any launch."""
+    big = 1024 + 1  # MHA_MAX_PADDED_BATCH + 1
+    assert _dec(lib, B=big) == 2
+    lens = (ctypes.c_int32 * big)(*([50] * big))
+    assert _dec(lib, B=big, lens=ctypes.cast(lens, ctypes.c_void_p)) == 2
+
+
 def test_decode_workspace_size(lib):
     from head_scaled_dot_gb300 import mha
     assert mha.decode_workspace_size(0, 1, 1, 1, 1) == 0
