@@ -46,6 +46,11 @@ struct DecodeParams {
   float cl2;       // c * log2(e)
   int causal_tail; // row i sees keys j <= L - n_q + i
   int valid_len[MHA_MAX_PADDED_BATCH];
+  // work items of the streaming kernel: (batch item, head, chunk), numbered
+  // batch item by batch item; item_start[b] = first item of batch item b
+  int nitems;
+  int item_start[MHA_MAX_PADDED_BATCH + 1];
+  uint64_t limit_ns;  // bounded waits give up after this long
 };
 
 template <typename T>
@@ -449,6 +454,254 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_partial_fast_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming pass 1 (bf16, d_h = d_vh = D in {64, 128}, up to 8 query rows).
+//
+// A persistent CTA walks work items (batch item, head, DEC_CHUNK-key chunk).
+// One producer thread copies each 32-key group of the cache, its K rows and
+// its V rows (contiguous in the head-split layout), into a DS_STAGES-deep
+// shared-memory ring with bulk asynchronous copies, as far ahead as the ring
+// allows and independently of the arithmetic, so that many groups' bytes are
+// in flight per SM. Consumer warp w takes groups n = w, w + DS_WARPS, ... of
+// the CTA's sequence, folds each into its own summary of the item's rows and
+// writes it as split chunk * DS_WARPS + w (an empty summary if it took no
+// group of the item), as decode_partial_kernel does.
+// ---------------------------------------------------------------------------
+
+constexpr int DS_WARPS = DEC_WARPS;  // consumer warps: same split count as pass 1
+constexpr int DS_THREADS = 32 * (DS_WARPS + 1);
+constexpr int DS_STAGES = 12;
+
+template <int NQ, int D>
+struct DsCfg {
+  static constexpr int ROW = D * 2;               // bytes of one K or V row
+  static constexpr int STAGE = 2 * 32 * ROW;      // K rows then V rows of a group
+  static constexpr int Q_FLOATS = NQ * D;         // one item's rows, fp32, pre-scaled
+  static constexpr int SMEM = DS_STAGES * STAGE + 2 * Q_FLOATS * 4 + 2 * DS_STAGES * 8 + 16;
+};
+
+// Batch item, head and chunk of work item `it`.
+__device__ __forceinline__ void ds_item(const DecodeParams& P, int it, int& b, int& head,
+                                        int& chunk) {
+  int lo = 0, hi = P.B - 1;
+  while (lo < hi) {  // last b with item_start[b] <= it
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.item_start[mid] <= it) lo = mid;
+    else hi = mid - 1;
+  }
+  b = lo;
+  const int local = it - P.item_start[b];
+  const int nch = (P.valid_len[b] + DEC_CHUNK - 1) / DEC_CHUNK;
+  head = local / nch;
+  chunk = local % nch;
+}
+
+// A bounded wait that ignores the abort flag: used only while draining copies
+// this CTA itself started, before it exits.
+__device__ __forceinline__ void ds_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if (globaltimer_ns() - t0 > 100000000ull) return;  // 100 ms
+  }
+}
+
+template <int NQ, int D>
+__global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
+    const __grid_constant__ DecodeParams P) {
+  using C = DsCfg<NQ, D>;
+  constexpr int CPL = D / 32;  // z columns per lane
+  constexpr int NCH = D / 8;   // 16-byte chunks of a row
+  extern __shared__ __align__(1024) uint8_t ds_smem[];
+  uint8_t* ring = ds_smem;  // [DS_STAGES][32 K rows | 32 V rows]
+  float* qs = reinterpret_cast<float*>(ring + DS_STAGES * C::STAGE);  // [2][NQ][D]
+  uint64_t* full = reinterpret_cast<uint64_t*>(qs + 2 * C::Q_FLOATS);
+  uint64_t* empty = full + DS_STAGES;
+  int* abort_flag = reinterpret_cast<int*>(empty + DS_STAGES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < DS_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl w{nullptr, abort_flag, P.limit_ns};
+  const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(P.K);
+  const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(P.V);
+
+  if (warp == DS_WARPS) {
+    if (lane == 0) {
+      // producer: group n of this CTA's sequence goes to stage n % DS_STAGES
+      uint32_t n = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < P.nitems && ok; it += gridDim.x) {
+        int b, head, chunk;
+        ds_item(P, it, b, head, chunk);
+        const int k0 = chunk * DEC_CHUNK, k1 = min(P.valid_len[b], k0 + DEC_CHUNK);
+        const long long row0 = ((long long)b * P.h + head) * P.n_k;
+        for (int k = k0; k < k1; k += 32, ++n) {
+          const int s = n % DS_STAGES;
+          if (n >= (uint32_t)DS_STAGES &&
+              !mbar_wait(&empty[s], ((n / DS_STAGES) - 1) & 1, w)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bytes = (uint32_t)min(32, k1 - k) * C::ROW;
+          uint8_t* dst = ring + s * C::STAGE;
+          mbar_arrive_expect_tx(&full[s], 2 * bytes);
+          bulk_copy_g2s(dst, Kg + (row0 + k) * D, bytes, &full[s]);
+          bulk_copy_g2s(dst + 32 * C::ROW, Vg + (row0 + k) * D, bytes, &full[s]);
+        }
+      }
+      if (!ok) {  // let the copies in flight land before the CTA exits
+        for (uint32_t k = (n > (uint32_t)DS_STAGES ? n - DS_STAGES : 0); k < n; ++k)
+          ds_drain(&full[k % DS_STAGES], (k / DS_STAGES) & 1);
+      }
+    }
+  } else {
+    const float cl2 = P.cl2;
+    uint32_t n = 0;
+    bool ok = true;
+    int ik = 0;  // items of this CTA so far
+    for (int it = blockIdx.x; it < P.nitems; it += gridDim.x, ++ik) {
+      int b, head, chunk;
+      ds_item(P, it, b, head, chunk);
+      const int L = P.valid_len[b];
+      const int k0 = chunk * DEC_CHUNK, k1 = min(L, k0 + DEC_CHUNK);
+      const long long bh = (long long)b * P.h + head;
+      // the item's query rows, pre-multiplied by c log2(e), shared by the
+      // consumer warps (double-buffered: a warp can only get here once every
+      // warp has passed the previous item's barrier, i.e. has finished the
+      // item before that, the last user of this buffer)
+      float* q = qs + (ik & 1) * C::Q_FLOATS;
+      const __nv_bfloat16* Qg = static_cast<const __nv_bfloat16*>(P.Q) + bh * P.n_q * D;
+      for (int e = threadIdx.x; e < C::Q_FLOATS; e += 32 * DS_WARPS)
+        q[e] = e < P.n_q * D ? __bfloat162float(Qg[e]) * cl2 : 0.f;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * DS_WARPS) : "memory");
+      float m_run[NQ], l_run[NQ], z_run[NQ][CPL];
+#pragma unroll
+      for (int r = 0; r < NQ; ++r) {
+        m_run[r] = -INFINITY;
+        l_run[r] = 0.f;
+#pragma unroll
+        for (int t = 0; t < CPL; ++t) z_run[r][t] = 0.f;
+      }
+      for (int k = k0; k < k1; k += 32, ++n) {
+        if ((int)(n % DS_WARPS) != warp) continue;
+        const int s = n % DS_STAGES;
+        // Stages are shared between consumer warps (DS_STAGES is not a
+        // multiple of DS_WARPS): before waiting for group n's phase of the
+        // stage, wait until group n - DS_STAGES (another warp's) has released
+        // it, so that the stage's barrier is never two phases behind the
+        // phase waited for (a parity wait cannot tell those apart). Group
+        // n - 2 DS_STAGES is this warp's own, so the release barrier is never
+        // two phases behind either.
+        if (ok && n >= (uint32_t)DS_STAGES &&
+            !mbar_wait(&empty[s], ((n / DS_STAGES) - 1) & 1, w))
+          ok = false;
+        if (ok && !mbar_wait(&full[s], (n / DS_STAGES) & 1, w)) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) {  // gave up: keep to the item loop, do no work
+          ok = false;
+          continue;
+        }
+        const int rows = min(32, k1 - k);
+        const uint8_t* kst = ring + s * C::STAGE;
+        const uint8_t* vst = kst + 32 * C::ROW;
+        // scores of this lane's key (row `lane` of the group) against every
+        // query row; lane j starts at 16-byte chunk j of its row, so the 32
+        // lanes' reads spread over the shared-memory banks
+        float sc[NQ];
+#pragma unroll
+        for (int r = 0; r < NQ; ++r) sc[r] = 0.f;
+        if (lane < rows) {
+          const uint8_t* krow = kst + lane * C::ROW;
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            const int c = (i + lane) & (NCH - 1);
+            float kv[8];
+            Vec16<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(krow + c * 16), kv);
+#pragma unroll
+            for (int r = 0; r < NQ; ++r) {
+              const float4 q0 = *reinterpret_cast<const float4*>(q + r * D + c * 8);
+              const float4 q1 = *reinterpret_cast<const float4*>(q + r * D + c * 8 + 4);
+              float acc = sc[r];
+              acc = fmaf(q0.x, kv[0], acc);
+              acc = fmaf(q0.y, kv[1], acc);
+              acc = fmaf(q0.z, kv[2], acc);
+              acc = fmaf(q0.w, kv[3], acc);
+              acc = fmaf(q1.x, kv[4], acc);
+              acc = fmaf(q1.y, kv[5], acc);
+              acc = fmaf(q1.z, kv[6], acc);
+              acc = fmaf(q1.w, kv[7], acc);
+              sc[r] = acc;
+            }
+          }
+        }
+        // fold the group into each row's summary (base 2)
+        const int key = k + lane;
+        float p[NQ];
+#pragma unroll
+        for (int r = 0; r < NQ; ++r) {
+          p[r] = 0.f;
+          if (r >= P.n_q) continue;  // uniform
+          bool allowed = lane < rows;
+          if (P.causal_tail) allowed = allowed && key <= L - P.n_q + r;
+          const float sv = allowed ? sc[r] : -INFINITY;
+          const float m_blk = dwarp_max(sv);
+          if (m_blk == -INFINITY) continue;  // the empty summary
+          const float m_new = fmaxf(m_run[r], m_blk);
+          const float a = exp2f(m_run[r] - m_new);
+          p[r] = allowed ? exp2f(sv - m_new) : 0.f;
+          l_run[r] = l_run[r] * a + dwarp_sum(p[r]);
+#pragma unroll
+          for (int t = 0; t < CPL; ++t) z_run[r][t] *= a;
+          m_run[r] = m_new;
+        }
+        // z += sum over the group's keys of p_j v_j; lane owns CPL columns
+        for (int j = 0; j < rows; ++j) {
+          float vv[CPL];
+          const uint8_t* vp = vst + j * C::ROW + lane * CPL * 2;
+          if constexpr (CPL == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(vp);
+            vv[0] = __uint_as_float(u.x << 16);
+            vv[1] = __uint_as_float(u.x & 0xffff0000u);
+            vv[2] = __uint_as_float(u.y << 16);
+            vv[3] = __uint_as_float(u.y & 0xffff0000u);
+          } else {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(vp);
+            vv[0] = __uint_as_float(u << 16);
+            vv[1] = __uint_as_float(u & 0xffff0000u);
+          }
+#pragma unroll
+          for (int r = 0; r < NQ; ++r) {
+            const float pj = __shfl_sync(0xffffffffu, p[r], j);
+#pragma unroll
+            for (int t = 0; t < CPL; ++t) z_run[r][t] = fmaf(pj, vv[t], z_run[r][t]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
+      }
+      // this warp's summaries of the item's rows (empty if it took no group)
+#pragma unroll
+      for (int r = 0; r < NQ; ++r) {
+        if (r >= P.n_q) continue;
+        float* dst = P.part + ((bh * P.n_q + r) * P.nsplit + chunk * DS_WARPS + warp) *
+                                  (long long)(2 + D);
+        if (lane == 0) {
+          dst[0] = m_run[r];
+          dst[1] = l_run[r];
+        }
+#pragma unroll
+        for (int t = 0; t < CPL; ++t) dst[2 + lane * CPL + t] = z_run[r][t];
+      }
+    }
+  }
+}
+
 // Pass 2. grid (n_q, h, B), 256 threads: merges the splits of one query row
 // (those below the valid length) and writes z / l.
 template <typename T>
@@ -528,9 +781,57 @@ bool launch_fast(const DecodeParams& P, const dim3& g1, cudaStream_t s) {
   return true;
 }
 
+template <int NQ, int D>
+bool launch_stream(const DecodeParams& P, cudaStream_t s) {
+  using C = DsCfg<NQ, D>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(decode_stream_kernel<NQ, D>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+      return false;
+    attr = true;
+  }
+  // as many CTAs as can be resident at once (shared memory and registers)
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<NQ, D>,
+                                                    DS_THREADS, C::SMEM) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int cap = num_sms() * per_sm;
+  const int grid = P.nitems < cap ? P.nitems : cap;
+  decode_stream_kernel<NQ, D><<<grid, DS_THREADS, C::SMEM, s>>>(P);
+  return true;
+}
+
+template <int D>
+bool launch_stream_rows(const DecodeParams& P, cudaStream_t s) {
+  if (P.n_q == 1) return launch_stream<1, D>(P, s);
+  if (P.n_q == 2) return launch_stream<2, D>(P, s);
+  if (P.n_q <= 4) return launch_stream<4, D>(P, s);
+  return launch_stream<8, D>(P, s);
+}
+
 template <typename T>
-mha_status launch_decode(const DecodeParams& P, int nchunk, cudaStream_t s) {
+mha_status launch_decode(DecodeParams& P, int nchunk, cudaStream_t s) {
   const dim3 g1(nchunk, P.h, P.B), g2(P.n_q, P.h, P.B);
+  if (sizeof(T) == 2 && P.d_h == P.d_vh && (P.d_h == 64 || P.d_h == 128) && P.n_q <= 8) {
+    // streaming pass 1: work items (batch item, head, chunk), batch item by
+    // batch item
+    long long items = 0;
+    for (int b = 0; b < P.B; ++b) {
+      P.item_start[b] = (int)items;
+      items += (long long)P.h * ((P.valid_len[b] + DEC_CHUNK - 1) / DEC_CHUNK);
+    }
+    if (items < (1ll << 30)) {
+      P.item_start[P.B] = (int)items;
+      P.nitems = (int)items;
+      const bool ok = P.d_h == 64 ? launch_stream_rows<64>(P, s) : launch_stream_rows<128>(P, s);
+      if (!ok) return MHA_ERR_CUDA;
+      decode_merge_kernel<T><<<g2, DEC_THREADS, 0, s>>>(P);
+      count_launch(2);
+      return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+    }
+  }
   if (launch_fast<T, 64, 64>(P, g1, s) || launch_fast<T, 128, 128>(P, g1, s)) {
     decode_merge_kernel<T><<<g2, DEC_THREADS, 0, s>>>(P);
     count_launch(2);
@@ -579,6 +880,8 @@ mha_status attention_decode(const DecodeArgs& a, mha_dtype dt, cudaStream_t s) {
   P.nsplit = nchunk * DEC_WARPS;
   P.cl2 = a.c * 1.4426950408889634f;
   P.causal_tail = a.causal_tail;
+  P.limit_ns = wait_limit_ns();
+  P.nitems = 0;
   for (int b = 0; b < MHA_MAX_PADDED_BATCH; ++b)
     P.valid_len[b] = (a.cache_len_host && b < a.B) ? a.cache_len_host[b] : a.n_k;
   if (dt == MHA_DTYPE_F32) return launch_decode<float>(P, nchunk, s);
