@@ -750,20 +750,33 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_merge_kernel(
   const float inv = 1.f / bcast;
   T* zrow = static_cast<T*>(P.Z) + ((long long)b * P.n_q + row) * (long long)P.h * dv +
             (long long)head * dv;
-  for (int col = threadIdx.x; col < dv; col += DEC_THREADS) {
-    float za[4] = {0.f, 0.f, 0.f, 0.f};
-    int s = 0;
-    for (; s + 4 <= nsp; s += 4) {
+  // z = sum_s w_s z_s, every thread busy: G groups of dv threads, group g
+  // summing the splits s = g, g + G, ..., eight loads in flight per thread;
+  // the groups' sums are then added through shared memory
+  __shared__ float zpart[DEC_THREADS];
+  const int G = DEC_THREADS / dv;  // d_vh <= 256: at least 1
+  const int col = threadIdx.x % dv, grp = threadIdx.x / dv;
+  float z = 0.f;
+  if (grp < G) {
+    float za[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int s = grp;
+    for (; s + 7 * G < nsp; s += 8 * G) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        za[u] = fmaf(w[s + u], src[(long long)(s + u) * (2 + dv) + 2 + col], za[u]);
+      for (int u = 0; u < 8; ++u)
+        za[u] = fmaf(w[s + u * G], src[(long long)(s + u * G) * (2 + dv) + 2 + col], za[u]);
     }
-    for (; s < nsp; ++s) za[0] = fmaf(w[s], src[(long long)s * (2 + dv) + 2 + col], za[0]);
-    const float z = (za[0] + za[1]) + (za[2] + za[3]);
+    for (; s < nsp; s += G) za[0] = fmaf(w[s], src[(long long)s * (2 + dv) + 2 + col], za[0]);
+    z = ((za[0] + za[1]) + (za[2] + za[3])) + ((za[4] + za[5]) + (za[6] + za[7]));
+  }
+  zpart[threadIdx.x] = z;
+  __syncthreads();
+  if (threadIdx.x < dv) {
+    float t = 0.f;
+    for (int g = 0; g < G; ++g) t += zpart[g * dv + threadIdx.x];
     if (sizeof(T) == 4)
-      reinterpret_cast<float*>(zrow)[col] = z * inv;
+      reinterpret_cast<float*>(zrow)[threadIdx.x] = t * inv;
     else
-      reinterpret_cast<__nv_bfloat16*>(zrow)[col] = __float2bfloat16_rn(z * inv);
+      reinterpret_cast<__nv_bfloat16*>(zrow)[threadIdx.x] = __float2bfloat16_rn(t * inv);
   }
 }
 
