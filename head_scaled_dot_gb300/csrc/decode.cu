@@ -804,11 +804,13 @@ bool launch_stream(const DecodeParams& P, cudaStream_t s) {
       return false;
     attr = true;
   }
-  // as many CTAs as can be resident at once (shared memory and registers)
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<NQ, D>,
-                                                    DS_THREADS, C::SMEM) != cudaSuccess ||
-      per_sm < 1)
+  // as many CTAs as can be resident at once (shared memory and registers),
+  // asked once
+  static int per_sm = 0;
+  if (per_sm < 1 &&
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<NQ, D>,
+                                                     DS_THREADS, C::SMEM) != cudaSuccess ||
+       per_sm < 1))
     per_sm = 1;
   const int cap = num_sms() * per_sm;
   const int grid = P.nitems < cap ? P.nitems : cap;
