@@ -2,9 +2,12 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
 
-One step is one whole forward pass (the error-word reset, the QKV projection
-with head split, the fused attention kernel and the output projection) over
-one batch of seeded synthetic inputs already resident in HBM. L2 is flushed
+One step is one whole forward pass (the QKV projection with head split, the
+fused attention kernel and the output projection) over one batch of seeded
+synthetic inputs already resident in HBM, timed as a whole with CUDA events
+around the three launches; the per-kernel split comes from as many further
+steps with events between the kernels (an event between two kernels keeps
+the second from starting its prologue under the first one's tail). L2 is flushed
 (a 512 MiB device write) between timed steps, outside the timed events. With
 N > 1 (torchrun) every rank runs an independent replica on its own GPU
 (replicas only: the forward pass has no exchange step), the time is the max
@@ -191,30 +194,35 @@ def measure_workload(w, steps, warmup, dev, world, e2e=True, sample_clocks=True)
 
     def step(ev):
         # the three kernels mha_forward enqueues (it also resets the 4-byte
-        # error word first), with events between them
+        # error word first); with four events, also between them (an event
+        # between two kernels keeps the second from starting its prologue
+        # under the first one's tail, so whole steps are timed with two)
+        split = len(ev) == 4
         ev[0].record(stream)
         rc = lib.mha_qkv_projection(P(t["X_q"].data_ptr()), X_kv_p, P(t["W_Q"].data_ptr()),
                                     P(t["W_K"].data_ptr()), P(t["W_V"].data_ptr()), P(Qp), P(Kp),
                                     P(Vp), B, n_q, n_k, w.d_model, w.h, w.d_h, w.d_vh, DT,
                                     P(err), sp)
-        ev[1].record(stream)
+        if split:
+            ev[1].record(stream)
         rc |= lib.mha_attention(P(Qp), P(Kp), P(Vp), P(Zp), B, n_q, n_k, w.h, w.d_h, w.d_vh,
                                 float(w.c), MK, lens_arg, 0 if w.cross else 1, DT, P(err), sp)
-        ev[2].record(stream)
+        if split:
+            ev[2].record(stream)
         rc |= lib.mha_output_projection(P(Zp), P(t["W_O"].data_ptr()), P(Y.data_ptr()), B, n_q,
                                         w.h, w.d_vh, w.d_o, DT, P(err), sp)
-        ev[3].record(stream)
+        ev[-1].record(stream)
         if rc != 0:
             raise RuntimeError("launch failed with status %d" % rc)
 
-    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    mk = lambda n=4: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     torch.cuda.synchronize(dev)
     ws[:4].zero_()
     for _ in range(warmup):
         flush.fill_(1.0)
         step(mk())
     torch.cuda.synchronize(dev)
-    events = [mk() for _ in range(steps)]
+    events = [mk(2) for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     # nvidia-smi samples every 200 ms, far longer than the timed steps: it
@@ -223,13 +231,13 @@ def measure_workload(w, steps, warmup, dev, world, e2e=True, sample_clocks=True)
     # see the clocks of this workload under load
     clocks = ClockSampler(dev.index if dev.index is not None else 0) if sample_clocks else None
     if clocks is not None:
-        spare = mk()
+        spare = mk(2)
         t_end = time.perf_counter() + CLOCK_WINDOW_S
         while time.perf_counter() < t_end:
             for _ in range(8):
                 flush.fill_(1.0)
                 step(spare)
-            spare[3].synchronize()
+            spare[-1].synchronize()
     launches0 = mha.launch_count()
     for ev in events:
         flush.fill_(1.0)  # L2 flush, outside the timed events
@@ -237,6 +245,12 @@ def measure_workload(w, steps, warmup, dev, world, e2e=True, sample_clocks=True)
     torch.cuda.synchronize(dev)
     barrier(world)
     launches = mha.launch_count() - launches0
+    # the per-kernel split, from as many further steps timed kernel by kernel
+    split_events = [mk() for _ in range(steps)]
+    for ev in split_events:
+        flush.fill_(1.0)
+        step(ev)
+    torch.cuda.synchronize(dev)
     clk = clocks.stop() if clocks is not None else None
     if clk is not None:
         clk["window_s"] = CLOCK_WINDOW_S
@@ -245,10 +259,11 @@ def measure_workload(w, steps, warmup, dev, world, e2e=True, sample_clocks=True)
         raise RuntimeError("device error word: %d" % status)
     per = {"qkv": [], "attention": [], "out": [], "step": []}
     for ev in events:
+        per["step"].append(ev[0].elapsed_time(ev[1]))
+    for ev in split_events:
         per["qkv"].append(ev[0].elapsed_time(ev[1]))
         per["attention"].append(ev[1].elapsed_time(ev[2]))
         per["out"].append(ev[2].elapsed_time(ev[3]))
-        per["step"].append(ev[0].elapsed_time(ev[3]))
     total_ms = sum(per["step"])
     fl = workcount.flops(w, lens)
     res = {"inputs": inp, "lens": lens, "flops": fl, "total_ms": total_ms, "per": per,

@@ -254,6 +254,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The prologue above touched only this CTA's shared and tensor memory. The
+  // next kernel may start its own now; this one reads its inputs and writes
+  // its outputs only once the previous kernel has completed.
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const WaitCtl w{P.err, abort_flag, P.limit_ns};
 
   if (warp < 4) {
@@ -763,9 +768,10 @@ mha_status launch(const AttnTcParams& P, int grid, cudaStream_t s) {
       return MHA_ERR_CUDA;
     attr = true;
   }
-  attn_tc_kernel<DQK, DV><<<grid, NTHREADS, C::SMEM, s>>>(P);
+  const cudaError_t e =
+      launch_dependent(attn_tc_kernel<DQK, DV>, dim3(grid), dim3(NTHREADS), C::SMEM, s, P);
   count_launch();
-  return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
 }  // namespace

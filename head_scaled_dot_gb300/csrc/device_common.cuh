@@ -400,6 +400,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Programmatic dependent launch. grid_dep_wait waits until the grid this one
+// depends on (the previous kernel of the stream, when this one was launched
+// with programmatic stream serialization) has completed and its memory is
+// visible; without such a launch it returns at once. grid_dep_launch_dependents
+// lets the next kernel of the stream start launching early: its CTAs run their
+// own prologue and then wait in grid_dep_wait.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
 __device__ __forceinline__ bool elect_one() {

@@ -99,6 +99,11 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The prologue above touched only this CTA's shared and tensor memory. The
+  // next kernel may start its own now; this one reads its inputs and writes
+  // its outputs only once the previous kernel has completed.
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const WaitCtl w{P.err, abort_flag, P.limit_ns};
   const int total = P.tile_start[P.nprob];
 
@@ -262,9 +267,9 @@ mha_status launch(GemmTcParams& P, cudaStream_t s) {
     attr_set = true;
   }
   const int grid = total < num_sms() ? total : num_sms();
-  gemm_tc_kernel<BN><<<grid, 192, C::SMEM, s>>>(P);
+  const cudaError_t e = launch_dependent(gemm_tc_kernel<BN>, dim3(grid), dim3(192), C::SMEM, s, P);
   count_launch();
-  return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
 }  // namespace

@@ -93,4 +93,23 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t
 
 mha_status selftest_wait(int32_t* err, uint64_t limit_ns, cudaStream_t s);
 
+// Launches kernel(arg) with programmatic stream serialization: it may begin
+// launching while the previous kernel of the stream is still running, and
+// must call grid_dep_wait before it reads or writes global memory.
+template <typename Arg>
+cudaError_t launch_dependent(void (*kernel)(Arg), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, const Arg& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
 }  // namespace mha
