@@ -93,6 +93,7 @@ constexpr int EXTRA = 512 + 2 * 2 * 128 * 4;
 
 template <int DQK, int DV>
 struct ACfg {
+  static constexpr int D_QK = DQK, D_V = DV;
   static constexpr int Q_TILE_BYTES = BLK_M * DQK * 2;
   static constexpr int K_BYTES = BLK_N * DQK * 2;
   static constexpr int V_BYTES = BLK_N * DV * 2;
@@ -198,6 +199,85 @@ __device__ __forceinline__ int unit_index(const AttnTcParams& P, int i) {
   return idx < P.units ? idx : -1;
 }
 
+// The shared-memory ring and barriers a TMA producer thread fills.
+struct Ring {
+  uint8_t* q_s;        // the two Q tiles
+  uint8_t* kv_s;       // STAGES x (K block, V block)
+  uint64_t* q_full;    // Q tiles of the current unit landed
+  uint64_t* q_empty;   // both tiles' S of the unit done with Q
+  uint64_t* k_full;    // [STAGES]
+  uint64_t* v_full;    // [STAGES]
+  uint64_t* k_empty;   // [STAGES]
+  uint64_t* v_empty;   // [STAGES]
+};
+
+// TMA producer thread of a persistent attention CTA. is_k: Q and the K blocks
+// (warp 0), else the V blocks (warp 2), unit after unit through the same
+// STAGES-deep ring (the ring position `it` runs on across units, so the next
+// unit's first blocks load while the current unit's last ones are still
+// being used); each also asks L2 for the blocks PREFETCH ahead so that
+// refills come from L2.
+template <class C>
+__device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bool is_k,
+                                        const WaitCtl& w) {
+  const CUtensorMap* map = is_k ? &P.kmap : &P.vmap;
+  uint64_t* full = is_k ? R.k_full : R.v_full;
+  uint64_t* empty = is_k ? R.k_empty : R.v_empty;
+  const int panels = is_k ? C::D_QK / 64 : C::D_V / 64;
+  const uint32_t bytes = is_k ? C::K_BYTES : C::V_BYTES;
+  tma_prefetch_desc(map);
+  if (is_k) tma_prefetch_desc(&P.qmap);
+  uint32_t it = 0;  // ring position
+  int ui = 0;       // units loaded so far
+  bool gave_up = false;
+  int q_last = -1;  // unit number of this thread's last Q load
+  for (int i = 0; !gave_up; ++i) {
+    const int idx = unit_index(P, i);
+    if (idx < 0) break;
+    const Unit u = unit_at(P, idx);
+    if (u.nmax == 0) continue;  // all rows padding: nothing to load
+    const int bh = u.b * P.h + u.head;
+    if (is_k) {
+      // the previous unit's S MMAs must be done reading the Q tiles
+      if (ui > 0 && !mbar_wait(R.q_empty, (ui - 1) & 1, w)) {
+        gave_up = true;
+        break;
+      }
+      const int ntiles = u.nb1 > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(R.q_full, ntiles * C::Q_TILE_BYTES);
+      for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+        for (int p = 0; p < C::D_QK / 64; ++p)
+          tma_load_3d(R.q_s + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, R.q_full, 64 * p,
+                      u.q0 + t * BLK_M, bh);
+      q_last = ui;
+    }
+    for (int kb = C::STAGES; kb < C::STAGES + PREFETCH && kb < u.nmax; ++kb)
+      for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, kb * BLK_N, bh);
+    for (int kb = 0; kb < u.nmax; ++kb, ++it) {
+      const int s = it % C::STAGES;
+      uint8_t* dst = R.kv_s + s * C::STAGE_BYTES + (is_k ? 0 : C::K_BYTES);
+      if (it >= (uint32_t)C::STAGES &&
+          !mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, w)) {
+        gave_up = true;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[s], bytes);
+      for (int p = 0; p < panels; ++p)
+        tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, kb * BLK_N, bh);
+      const int ahead = kb + C::STAGES + PREFETCH;
+      if (ahead < u.nmax)
+        for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, ahead * BLK_N, bh);
+    }
+    ++ui;
+  }
+  if (gave_up) {  // let this thread's loads land before the CTA exits
+    if (is_k && q_last >= 0) drain(R.q_full, q_last & 1);
+    for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
+      drain(&full[k % C::STAGES], (k / C::STAGES) & 1);
+  }
+}
+
 template <int DQK, int DV>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
@@ -260,71 +340,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   grid_dep_launch_dependents();
   grid_dep_wait();
   const WaitCtl w{P.err, abort_flag, P.limit_ns};
+  const Ring ring{q_s, kv_s, q_full, q_empty, k_full, v_full, k_empty, v_empty};
 
   if (warp < 4) {
     if ((warp == 0 || warp == 2) && lane == 0) {
-      // warp 0 streams Q and the K blocks, warp 2 the V blocks, unit after
-      // unit through the same STAGES-deep ring (the ring position `it` runs
-      // on across units, so the next unit's first blocks load while the
-      // current unit's last ones are still being used); each also asks L2
-      // for the blocks PREFETCH ahead so that refills come from L2
-      const bool is_k = warp == 0;
-      const CUtensorMap* map = is_k ? &P.kmap : &P.vmap;
-      uint64_t* full = is_k ? k_full : v_full;
-      uint64_t* empty = is_k ? k_empty : v_empty;
-      const int panels = is_k ? DQK / 64 : DV / 64;
-      const uint32_t bytes = is_k ? C::K_BYTES : C::V_BYTES;
-      tma_prefetch_desc(map);
-      if (is_k) tma_prefetch_desc(&P.qmap);
-      uint32_t it = 0;  // ring position
-      int ui = 0;       // units loaded so far
-      bool gave_up = false;
-      int q_last = -1;         // unit number of this thread's last Q load
-      for (int i = 0; !gave_up; ++i) {
-        const int idx = unit_index(P, i);
-        if (idx < 0) break;
-        const Unit u = unit_at(P, idx);
-        if (u.nmax == 0) continue;  // all rows padding: nothing to load
-        const int bh = u.b * P.h + u.head;
-        if (is_k) {
-          // the previous unit's S MMAs must be done reading the Q tiles
-          if (ui > 0 && !mbar_wait(q_empty, (ui - 1) & 1, w)) {
-            gave_up = true;
-            break;
-          }
-          const int ntiles = u.nb1 > 0 ? 2 : 1;
-          mbar_arrive_expect_tx(q_full, ntiles * C::Q_TILE_BYTES);
-          for (int t = 0; t < ntiles; ++t)
-#pragma unroll
-            for (int p = 0; p < DQK / 64; ++p)
-              tma_load_3d(q_s + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, q_full, 64 * p,
-                          u.q0 + t * BLK_M, bh);
-          q_last = ui;
-        }
-        for (int kb = C::STAGES; kb < C::STAGES + PREFETCH && kb < u.nmax; ++kb)
-          for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, kb * BLK_N, bh);
-        for (int kb = 0; kb < u.nmax; ++kb, ++it) {
-          const int s = it % C::STAGES;
-          uint8_t* dst = kv_s + s * C::STAGE_BYTES + (is_k ? 0 : C::K_BYTES);
-          if (it >= (uint32_t)C::STAGES &&
-              !mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, w)) {
-            gave_up = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[s], bytes);
-          for (int p = 0; p < panels; ++p)
-            tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, kb * BLK_N, bh);
-          const int ahead = kb + C::STAGES + PREFETCH;
-          if (ahead < u.nmax)
-            for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, ahead * BLK_N, bh);
-        }
-        ++ui;
-      }
-      if (gave_up) {  // let this thread's loads land before the CTA exits
-        if (is_k && q_last >= 0) drain(q_full, q_last & 1);
-        for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
-          drain(&full[k % C::STAGES], (k / C::STAGES) & 1);
-      }
+      produce<C>(P, ring, warp == 0, w);
     } else if ((warp == 1 || warp == 3) && lane == 0) {
       // Two MMA issuers, one per query tile (warp 1: tile 0, warp 3: tile 1).
       // Each keeps its own short tensor-instruction queue filled, so the
@@ -659,6 +679,386 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Variant for d_vh = 64: S, P and z of both tiles in separate TMEM columns
+// (S 2 x 128, P 2 x 64 as bf16 pairs, z 2 x 64 = 512). A tile's next S can
+// then be computed as soon as its softmax warps have read the current S
+// into registers (s_free), while they still work on it, instead of after the
+// tile's P V; and each tile has its own eight softmax warps, so one tile's
+// softmax latency (loads, exchange, barrier waits) overlaps the other's
+// exponentials. P is overwritten only once the previous block's P V is done.
+// ---------------------------------------------------------------------------
+
+constexpr int SP_THREADS = 128 + 2 * 256;  // 4 control warps, 8 softmax warps per tile
+
+template <int DQK>
+struct SpCfg {
+  static constexpr int D_QK = DQK, D_V = 64;
+  static constexpr int Q_TILE_BYTES = BLK_M * DQK * 2;
+  static constexpr int K_BYTES = BLK_N * DQK * 2;
+  static constexpr int V_BYTES = BLK_N * 64 * 2;
+  static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
+  // barriers (up to 64 x 8 B), then the exchange [2 tiles][2 halves][2 slots][128]
+  static constexpr int EXTRA_SP = 512 + 2 * 2 * 2 * 128 * 4;
+  static constexpr int BUDGET = 227 * 1024 - 2 * Q_TILE_BYTES - 1024 - EXTRA_SP;
+  static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 4 ? 4 : (BUDGET / STAGE_BYTES);
+  static constexpr int SMEM = 2 * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA_SP;
+  // TMEM columns of tile t: S at 128 t, P at 256 + 64 t, z at 384 + 64 t
+  static constexpr uint32_t S_COL = 0, P_COL = 256, O_COL = 384;
+  static_assert(STAGES >= 2, "shared memory");
+};
+
+template <int DQK>
+__global__ void __launch_bounds__(SP_THREADS, 1)
+    attn_tc_sp_kernel(const __grid_constant__ AttnTcParams P) {
+  using C = SpCfg<DQK>;
+  constexpr int DV = 64;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  __nv_bfloat16* Zg = static_cast<__nv_bfloat16*>(P.Z);
+  const long long zrow_stride = (long long)P.h * DV;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* q_s = smem;
+  uint8_t* kv_s = smem + 2 * C::Q_TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + C::STAGES * C::STAGE_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* k_full = q_empty + 1;           // [STAGES]
+  uint64_t* v_full = k_full + C::STAGES;    // [STAGES]
+  uint64_t* k_empty = v_full + C::STAGES;   // [STAGES]
+  uint64_t* v_empty = k_empty + C::STAGES;  // [STAGES]
+  uint64_t* s_full = v_empty + C::STAGES;   // [2] S of the block is in TMEM
+  uint64_t* s_free = s_full + 2;            // [2] the softmax warps have read S
+  uint64_t* p_full = s_free + 2;            // [2] P of the block is in TMEM
+  uint64_t* o_full = p_full + 2;            // [2] z += P V done
+  uint64_t* o_empty = o_full + 2;           // [2] z read out by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 2);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  float* xchg = reinterpret_cast<float*>(bars + 64);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 2);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 2);
+      mbar_init(&v_empty[s], 2);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 8);   // one arrival per softmax warp of the tile
+      mbar_init(&p_full[t], 8);
+      mbar_init(&o_full[t], 1);
+      mbar_init(&o_empty[t], 8);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_launch_dependents();
+  grid_dep_wait();
+  const WaitCtl w{P.err, abort_flag, P.limit_ns};
+  const Ring ring{q_s, kv_s, q_full, q_empty, k_full, v_full, k_empty, v_empty};
+
+  if (warp < 4) {
+    if ((warp == 0 || warp == 2) && lane == 0) {
+      produce<C>(P, ring, warp == 0, w);
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+      // MMA issuer of tile t. Order per tile: S_0, S_1 (once S_0 is read),
+      // P_0 V, S_2 (once S_1 is read), P_1 V, ...; S_{j+1} does not wait for
+      // P_j V because P has columns of its own.
+      const int t = warp == 1 ? 0 : 1;
+      const uint32_t idesc_qk =
+          idesc_bf16_f32(BLK_M, BLK_N, 0, 0) | (P.negate ? (1u << 13) : 0u);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BLK_M, DV, 0, 1);
+      const uint64_t qd = sdesc_sw128(smem_u32(q_s + t * C::Q_TILE_BYTES), 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(smem_u32(kv_s), 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(smem_u32(kv_s + C::K_BYTES), 16384, 1024);
+      constexpr uint64_t STAGE_D = C::STAGE_BYTES >> 4;
+      const uint32_t s_tmem = tmem + C::S_COL + 128 * t;
+      const uint32_t p_tmem = tmem + C::P_COL + 64 * t;
+      const uint32_t o_tmem = tmem + C::O_COL + 64 * t;
+      auto issue_s = [&](uint32_t r) {
+        const uint64_t kd = k_desc + (uint64_t)(r % C::STAGES) * STAGE_D;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+          umma_ss(s_tmem, qd + off, kd + off, idesc_qk, kk > 0);
+        }
+        umma_commit(&s_full[t]);
+        umma_commit(&k_empty[r % C::STAGES]);
+      };
+      auto issue_pv = [&](uint32_t r, bool first) {
+        const uint64_t vd = v_desc + (uint64_t)(r % C::STAGES) * STAGE_D;
+#pragma unroll
+        for (int kk = 0; kk < BLK_N / 16; ++kk)
+          umma_ts(o_tmem, p_tmem + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                  (!first || kk > 0));
+        umma_commit(&o_full[t]);
+        umma_commit(&v_empty[r % C::STAGES]);
+      };
+      uint32_t base = 0;  // ring position of the current unit's block 0
+      uint32_t cs = 0;    // S issued for this tile so far (s_full / s_free phases)
+      uint32_t c = 0;     // P V issued for this tile so far (p_full / o_full phases)
+      uint32_t act = 0;   // units in which this tile had rows to compute
+      int ui = 0;
+      bool ok = true, inflight = false;
+      // S number cs may be issued once S number cs - 1 has been read out
+      auto s_slot_free = [&]() { return cs == 0 || mbar_wait(&s_free[t], (cs - 1) & 1, w); };
+      for (int i = 0; ok; ++i) {
+        const int idx = unit_index(P, i);
+        if (idx < 0) break;
+        const Unit u = unit_at(P, idx);
+        if (u.nmax == 0) continue;
+        const int nbt = t ? u.nb1 : u.nb0;
+        if (!mbar_wait(q_full, ui & 1, w)) {
+          ok = false;
+          break;
+        }
+        if (nbt > 0) {
+          if (!s_slot_free() ||
+              !mbar_wait(&k_full[base % C::STAGES], (base / C::STAGES) & 1, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(base);
+          ++cs;
+          inflight = true;
+          if (nbt == 1) umma_commit(q_empty);  // the unit's last S is issued
+          for (int kb = 0; kb < nbt; ++kb, ++c) {
+            const uint32_t r = base + kb;
+            if (kb + 1 < nbt) {
+              if (!s_slot_free() ||
+                  !mbar_wait(&k_full[(r + 1) % C::STAGES], ((r + 1) / C::STAGES) & 1, w)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(r + 1);
+              ++cs;
+              if (kb + 2 == nbt) umma_commit(q_empty);
+            }
+            if (!mbar_wait(&v_full[r % C::STAGES], (r / C::STAGES) & 1, w) ||
+                !mbar_wait(&p_full[t], c & 1, w) ||
+                (kb == 0 && act > 0 && !mbar_wait(&o_empty[t], (act - 1) & 1, w))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(r, kb == 0);
+          }
+          if (!ok) break;
+          ++act;
+        } else {
+          mbar_arrive(q_empty);  // this tile has no rows in the unit: no S reads Q
+        }
+        for (int k2 = nbt; k2 < u.nmax && ok; ++k2) {
+          const uint32_t r = base + k2;
+          const int s = r % C::STAGES;
+          const uint32_t par = (r / C::STAGES) & 1;
+          if (!mbar_wait(&k_full[s], par, w)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive(&k_empty[s]);
+          if (!mbar_wait(&v_full[s], par, w)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive(&v_empty[s]);
+        }
+        base += u.nmax;
+        ++ui;
+      }
+      if (!ok && inflight) {  // gave up: wait for this thread's MMAs before TMEM is released
+        umma_commit(&s_full[t]);
+        drain(&s_full[t], 0);
+        drain(&s_full[t], 1);
+      }
+    }
+  } else {
+    // Softmax: warps 4..11 own tile 0, warps 12..19 tile 1. A row is split
+    // between the two warps of its tile that see the same TMEM lane slice
+    // (`half`: key columns [64 half, 64 half + 64) of S, z columns
+    // [32 half, 32 half + 32)); the partners combine their partial row max
+    // through shared memory under a 64-thread named barrier.
+    const int t = (warp - 4) >> 3;
+    const int half = ((warp - 4) >> 2) & 1;
+    const int g = warp & 3;  // TMEM lane slice 32*g .. 32*g+31
+    const int r = 32 * g + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * g) << 16;
+    const uint32_t s_addr = tmem + lane_off + C::S_COL + 128 * t;
+    const uint32_t p_addr = tmem + lane_off + C::P_COL + 64 * t;
+    const uint32_t o_addr = tmem + lane_off + C::O_COL + 64 * t;
+    const float cl2 = P.cl2;
+    const float2 cl2x2 = make_float2(cl2, cl2);
+    const int xo = 256 * (2 * t + half) + r;      // this thread's exchange slots
+    const int po = 256 * (2 * t + 1 - half) + r;  // the partner's
+    auto pair_sync = [&]() {
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + 4 * t + g) : "memory");
+    };
+    uint32_t cS = 0;  // blocks of this tile folded so far (s_full / s_free / p_full / o_full)
+    int xc = 0;       // exchanges so far (alternates the shared slots)
+    bool ok = true;
+    for (int i = 0;; ++i) {
+      const int idx = unit_index(P, i);
+      if (idx < 0) break;
+      const Unit u = unit_at(P, idx);
+      if (t == 1 && !u.pair) continue;  // a single-tile unit: those rows are another unit's
+      const int nblk = t ? u.nb1 : u.nb0;
+      const int tq0 = u.q0 + t * BLK_M;
+      const int q = tq0 + r;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int kb = 0; kb < nblk; ++kb) {
+        const uint32_t cc = cS++;
+        if (ok && !mbar_wait(&s_full[t], cc & 1, w)) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) {  // keep the pair in step, do no work
+          ok = false;
+          pair_sync();
+          ++xc;
+          continue;
+        }
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(s_addr + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(s_addr + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_wait_ld();
+        // S is in registers: the tile's next S may be computed into its columns
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[t]);
+        const int k0 = kb * BLK_N;
+        const bool masked = (k0 + BLK_N > u.L) || (P.causal && k0 + BLK_N - 1 > tq0);
+        const int lim = (masked ? (P.causal ? min(u.L, q + 1) : u.L) - k0 : BLK_N) - 64 * half;
+        if (masked) {
+          // forbidden keys get s = -inf, hence weight 2^{-inf} = 0 exactly
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
+        }
+        xchg[xo + 128 * (xc & 1)] = max64(sr);
+        pair_sync();
+        const float mx = fmaxf(xchg[xo + 128 * (xc & 1)], xchg[po + 128 * (xc & 1)]);
+        ++xc;
+        const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
+        // raise the running max only past the threshold (or on the first block)
+        const bool raise = (m_run == -INFINITY) ? true : (m_blk > m_run + RESCALE_LOG2);
+        const float m_new = raise ? fmaxf(m_run, m_blk) : m_run;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2_approx(m_run - m_use);  // e^{m - m'}: 1 when m is kept
+        const float2 negm = make_float2(-m_use, -m_use);
+        // p = 2^{c log2(e) s - m}, all 64 of this half row into registers
+        float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          float2 x0 = __ffma2_rn(
+              make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), cl2x2, negm);
+          float2 x1 = __ffma2_rn(
+              make_float2(__uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3])), cl2x2, negm);
+          x0.x = ex2_approx(x0.x);
+          x0.y = ex2_approx(x0.y);
+          x1.x = ex2_approx(x1.x);
+          x1.y = ex2_approx(x1.y);
+          sum = __fadd2_rn(sum, x0);
+          sum_b = __fadd2_rn(sum_b, x1);
+          pk[j / 2] = pack_bf16x2(x0.x, x0.y);
+          pk[j / 2 + 1] = pack_bf16x2(x1.x, x1.y);
+        }
+        l_run = l_run * alpha + ((sum.x + sum.y) + (sum_b.x + sum_b.y));
+        // the previous block's z += P V must be done before P is overwritten
+        // (and before z is rescaled); by now it normally is
+        if (kb > 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&o_full[t], (cc - 1) & 1, w))) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+        }
+        tmem_st16(p_addr + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(p_addr + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        if (__any_sync(0xffffffffu, kb > 0 && raise)) {
+          // merge: rescale this half row of z by e^{m - m'}
+          uint32_t o[32];
+          tmem_ld32(o_addr + 32 * half, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 v =
+                __fmul2_rn(make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
+                           make_float2(alpha, alpha));
+            o[j] = __float_as_uint(v.x);
+            o[j + 1] = __float_as_uint(v.y);
+          }
+          tmem_st32(o_addr + 32 * half, o);
+        }
+        m_run = m_new;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
+      }
+      // Epilogue of the unit: z / l for this half of each row
+      __nv_bfloat16* zrow = Zg + (long long)u.b * P.n_q * zrow_stride + (long long)u.head * DV +
+                            (long long)q * zrow_stride + 32 * half;
+      if (nblk == 0) {
+        if (q < P.n_q) {  // the whole tile is padding: its rows are zero
+#pragma unroll
+          for (int j = 0; j < 4; ++j) reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      xchg[xo + 128 * (xc & 1)] = l_run;
+      pair_sync();
+      const float l_tot = l_run + xchg[po + 128 * (xc & 1)];
+      ++xc;
+      if (!ok || !__all_sync(0xffffffffu, mbar_wait(&o_full[t], (cS - 1) & 1, w))) {
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+      const bool computed = q < u.q_end;
+      const float inv = computed ? P.head_gate[u.head] / l_tot : 0.f;
+      uint32_t o[32];
+      tmem_ld32(o_addr + 32 * half, o);
+      tmem_wait_ld();
+      if (q < P.n_q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = computed ? pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
+                                         __uint_as_float(o[2 * j + 1]) * inv)
+                           : 0u;
+        uint4* dst = reinterpret_cast<uint4*>(zrow);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[t]);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 // Host side of the schedule. The cost of a unit is counted in tile steps
 // (one 128 x 128 block of one tile); each CTA also pays a fixed part per unit
 // that it cannot overlap: in a CTA of its own, the start-up (loads, first S)
@@ -774,6 +1174,22 @@ mha_status launch(const AttnTcParams& P, int grid, cudaStream_t s) {
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
+template <int DQK>
+mha_status launch_sp(const AttnTcParams& P, int grid, cudaStream_t s) {
+  using C = SpCfg<DQK>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_tc_sp_kernel<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
+      return MHA_ERR_CUDA;
+    attr = true;
+  }
+  const cudaError_t e =
+      launch_dependent(attn_tc_sp_kernel<DQK>, dim3(grid), dim3(SP_THREADS), C::SMEM, s, P);
+  count_launch();
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
 }  // namespace
 
 mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
@@ -817,10 +1233,11 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
     P.head_gate[i] = (a.head_gate_host && i < a.h) ? a.head_gate_host[i] : 1.f;
   // one CTA per unit, or one persistent CTA per SM walking its share
   const int grid = choose_schedule(P, a.B, a.d_h, a.d_vh);
-  if (a.d_h == 64 && a.d_vh == 64) return launch<64, 64>(P, grid, s);
+  // d_vh = 64: S, P and z fit in separate TMEM columns
+  if (a.d_h == 64 && a.d_vh == 64) return launch_sp<64>(P, grid, s);
   if (a.d_h == 128 && a.d_vh == 128) return launch<128, 128>(P, grid, s);
   if (a.d_h == 64 && a.d_vh == 128) return launch<64, 128>(P, grid, s);
-  if (a.d_h == 128 && a.d_vh == 64) return launch<128, 64>(P, grid, s);
+  if (a.d_h == 128 && a.d_vh == 64) return launch_sp<128>(P, grid, s);
   return MHA_ERR_UNSUPPORTED;
 }
 
