@@ -1067,7 +1067,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
 // under the current unit's last steps).
 constexpr int UNIT_FIXED = 5, PERSIST_FIXED = 2;
 constexpr long long MAX_SIMULATED_UNITS = 1 << 16;
-constexpr double PI_MAJOR_MAX_KV_BYTES = 96.0 * (1 << 20);  // K and V kept in L2
+constexpr double PI_MAJOR_MAX_KV_BYTES = 112.0 * (1 << 20);  // K and V read, kept in L2
 
 // A tile on its own cannot overlap its softmax with its MMAs: a step costs
 // the softmax plus the MMAs, about 1 + 4 (d_h + d_vh) / 1600 pair steps.
@@ -1142,20 +1142,28 @@ int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh) {
     return G;
   }
   if (pairs > MAX_SIMULATED_UNITS) return pairs;
-  const double one_each = per_unit_makespan(P, G, sr);
-  double best = persistent_makespan(P, G, sr);
-  int best_pi_major = 0;
-  const double kv_bytes = (double)B * P.h * P.n_k * (d_h + d_vh) * 2.0;
-  if (P.causal && kv_bytes <= PI_MAJOR_MAX_KV_BYTES) {
-    P.pi_major = 1;
-    const double t = persistent_makespan(P, G, sr);
-    if (t < best) {
+  // the four schedules: one CTA per unit or persistent CTAs, units pair by
+  // pair within each head or heavy causal pairs of all heads first (only
+  // when the K and V that will be read stay in L2)
+  double kv_bytes = 0;
+  for (int b = 0; b < B; ++b)
+    kv_bytes += (double)(P.padding ? P.valid_len[b] : P.n_k) * P.h * (d_h + d_vh) * 2.0;
+  const bool pm_ok = P.causal && kv_bytes <= PI_MAJOR_MAX_KV_BYTES;
+  double best = 0;
+  int best_grid = pairs, best_pm = 0;
+  for (int pm = 0; pm <= (pm_ok ? 1 : 0); ++pm) {
+    P.pi_major = pm;
+    const double one_each = per_unit_makespan(P, G, sr);
+    const double persistent = persistent_makespan(P, G, sr);
+    const double t = persistent < one_each ? persistent : one_each;
+    if (pm == 0 || t < best) {
       best = t;
-      best_pi_major = 1;
+      best_grid = persistent < one_each ? G : pairs;
+      best_pm = pm;
     }
   }
-  P.pi_major = best < one_each ? best_pi_major : 0;
-  return best < one_each ? G : P.units;
+  P.pi_major = best_pm;
+  return best_grid;
 }
 
 template <int DQK, int DV>
