@@ -9,22 +9,27 @@
 // and writes z / l once per row. The n_q x n_k score matrix only ever exists
 // as one 128 x 128 block per tile, in tensor memory (TMEM).
 //
-// Roles (384 threads, three warpgroups):
-//   warps 0, 2    TMA producers: warp 0 loads both Q tiles once and the K
-//                 blocks, warp 2 the V blocks, into a STAGES-deep ring (K and
-//                 V freed separately); each also prefetches the blocks a few
-//                 steps ahead into L2
+// Two kernels share the units, the schedule and the TMA producers:
+//
+// attn_tc_kernel<DQK, DV> (d_vh = 128; 384 threads):
+//   warps 0, 2    TMA producers: warp 0 loads the Q tiles of each unit and the
+//                 K blocks, warp 2 the V blocks, into a STAGES-deep ring (K
+//                 and V freed separately); each also prefetches the blocks a
+//                 few steps ahead into L2
 //   warps 1, 3    MMA issuers, one per tile t: S_t = Q_t K_j^T (SMEM x SMEM
 //                 -> TMEM) and z_t += P_t V_j (P from TMEM, V from SMEM); the
 //                 two tiles' streams interleave on the tensor pipe, so one
 //                 tile's softmax overlaps the other tile's MMAs
-//   warps 4..7    softmax of tile 0, warps 8..11 softmax of tile 1: thread =
-//                 query row = TMEM lane. It reads its row of S from TMEM, takes
-//                 the row max in-thread (a TMEM lane holds a whole row: no
-//                 shuffles),
-//                 computes p = 2^{c log2(e) s - m}, writes p as bf16 over the
-//                 columns of S (P aliases S), and at the end writes z / l in
-//                 the concatenated (B, n_q, h*d_vh) layout.
+//   warps 4..11   softmax, tile 0 then tile 1 of every key block; a row is
+//                 split over the two warps that see its TMEM lane (64 keys
+//                 each, partial maxima exchanged through shared memory); p is
+//                 written as bf16 over the columns of S (P aliases S), and z / l
+//                 at the end of the unit in the concatenated layout
+//
+// attn_tc_sp_kernel<DQK> (d_vh = 64; 640 threads): the same roles, but S, P
+// and z of both tiles have TMEM columns of their own and each tile has its
+// own eight softmax warps (warps 4..11 tile 0, 12..19 tile 1), so a tile's
+// next S is computed while its softmax still works on the current one.
 //
 // Stale maximum: the running m of a row is only raised when a block's max
 // exceeds it by more than 2^8 (then z and l are rescaled by e^{m - m'} in
@@ -36,17 +41,19 @@
 // Key blocks that are fully masked (past the causal diagonal, past the valid
 // length) are never loaded: they are the empty summary.
 //
-// Schedule. A unit is one tile pair of one (batch item, head). With no more
-// units than SMs every CTA takes one unit. Otherwise the host estimates two
-// schedules from the per-unit block counts (causal diagonal, valid lengths)
-// and launches the faster: one CTA per unit, handed out by the hardware in
-// order, or one persistent CTA per SM that walks a fixed list of units
-// (rounds of one unit per CTA, the CTA order reversed on odd rounds), with
-// the heavy causal pairs of every head first when K and V stay in L2. In a
-// persistent CTA the barrier phases run on from unit to unit: the next unit's
-// Q waits for the current unit's last S (q_empty), its first z = P V for the
-// epilogue to read the current z out (o_empty), and its K/V loads and first S
-// overlap the current unit's last blocks and epilogue.
+// Schedule. A unit is one tile pair of one (batch item, head), or a single
+// tile. With no more units than SMs every CTA takes one unit. Otherwise the
+// host estimates, from the per-unit block counts (causal diagonal, valid
+// lengths), one CTA per unit (handed out by the hardware in order) and one
+// persistent CTA per SM that walks a fixed list of units (rounds of one unit
+// per CTA, the CTA order reversed on odd rounds), each with the units pair
+// by pair within a head or with the heavy causal pairs of all heads first
+// (when the K and V to be read stay in L2), and launches the fastest;
+// without a mask the pairs of a last, partly filled round may run as single
+// tiles. In a persistent CTA the barrier phases run on from unit to unit: the
+// next unit's Q waits for the current unit's last S (q_empty), its first
+// z = P V for the epilogue to read the current z out (o_empty), and its K/V
+// loads and first S overlap the current unit's last blocks and epilogue.
 #include <cuda_bf16.h>
 #include <math.h>
 
