@@ -137,7 +137,10 @@ MHA_API mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h,
  * Head sizes d_h, d_vh from 1 to 256 (MHA_ERR_UNSUPPORTED otherwise); bf16
  * heads of 64 or 128 run on the tensor cores, other sizes on CUDA cores.
  * bf16 also needs d_model, d_h, d_vh and d_o to be multiples of 8.
- * Enqueues a 4-byte memset of the error word and three kernels.
+ * Enqueues a 4-byte memset of the error word and three kernels. Everything
+ * it enqueues is stream-ordered, so the call can be captured in a CUDA graph
+ * on fixed buffers and replayed; host-side arguments (sizes, c, valid_len)
+ * are read at capture time and stay fixed in the replays.
  */
 MHA_API mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q,
                        const void* W_K, const void* W_V, const void* W_O,
