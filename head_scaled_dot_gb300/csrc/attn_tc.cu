@@ -50,10 +50,12 @@
 // by pair within a head or with the heavy causal pairs of all heads first
 // (when the K and V to be read stay in L2), and launches the fastest;
 // without a mask the pairs of a last, partly filled round may run as single
-// tiles. In a persistent CTA the barrier phases run on from unit to unit: the
-// next unit's Q waits for the current unit's last S (q_empty), its first
-// z = P V for the epilogue to read the current z out (o_empty), and its K/V
-// loads and first S overlap the current unit's last blocks and epilogue.
+// tiles. In a persistent CTA the barrier phases run on from unit to unit: a
+// unit's Q waits for the last S of the unit that used its Q buffer before
+// (q_empty; at d_h = 64 there are two buffers, so the next unit's Q loads
+// while the current unit runs), its first z = P V for the epilogue to read
+// the current z out (o_empty), and its K/V loads and first S overlap the
+// current unit's last blocks and epilogue.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -107,6 +109,7 @@ struct ACfg {
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
   static constexpr int BUDGET = 227 * 1024 - 2 * Q_TILE_BYTES - 1024 - EXTRA;
   static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 4 ? 4 : (BUDGET / STAGE_BYTES);
+  static constexpr int Q_BUFS = 1;  // Q tile pairs in shared memory
   static constexpr int SMEM = 2 * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA;
   // TMEM columns: S of tile 0 and 1, then z (O) of tile 0 and 1.
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
@@ -208,10 +211,10 @@ __device__ __forceinline__ int unit_index(const AttnTcParams& P, int i) {
 
 // The shared-memory ring and barriers a TMA producer thread fills.
 struct Ring {
-  uint8_t* q_s;        // the two Q tiles
+  uint8_t* q_s;        // Q_BUFS x the two Q tiles (unit i uses buffer i % Q_BUFS)
   uint8_t* kv_s;       // STAGES x (K block, V block)
-  uint64_t* q_full;    // Q tiles of the current unit landed
-  uint64_t* q_empty;   // both tiles' S of the unit done with Q
+  uint64_t* q_full;    // [Q_BUFS] Q tiles of a unit landed
+  uint64_t* q_empty;   // [Q_BUFS] both tiles' S of the unit done with Q
   uint64_t* k_full;    // [STAGES]
   uint64_t* v_full;    // [STAGES]
   uint64_t* k_empty;   // [STAGES]
@@ -245,22 +248,22 @@ __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bo
     if (u.nmax == 0) continue;  // all rows padding: nothing to load
     const int bh = u.b * P.h + u.head;
     if (is_k) {
-      // the previous unit's S MMAs must be done reading the Q tiles
-      if (ui > 0 && !mbar_wait(R.q_empty, (ui - 1) & 1, w)) {
+      // the S MMAs of the unit that last used this Q buffer must be done
+      const int qb = ui % C::Q_BUFS;
+      if (ui >= C::Q_BUFS && !mbar_wait(R.q_empty + qb, (ui / C::Q_BUFS - 1) & 1, w)) {
         gave_up = true;
         break;
       }
       const int ntiles = u.nb1 > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(R.q_full, ntiles * C::Q_TILE_BYTES);
+      uint8_t* q_dst = R.q_s + qb * 2 * C::Q_TILE_BYTES;
+      mbar_arrive_expect_tx(R.q_full + qb, ntiles * C::Q_TILE_BYTES);
       for (int t = 0; t < ntiles; ++t)
 #pragma unroll
         for (int p = 0; p < C::D_QK / 64; ++p)
-          tma_load_3d(R.q_s + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, R.q_full, 64 * p,
+          tma_load_3d(q_dst + t * C::Q_TILE_BYTES + p * 16384, &P.qmap, R.q_full + qb, 64 * p,
                       u.q0 + t * BLK_M, bh);
       q_last = ui;
     }
-    for (int kb = C::STAGES; kb < C::STAGES + PREFETCH && kb < u.nmax; ++kb)
-      for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, kb * BLK_N, bh);
     for (int kb = 0; kb < u.nmax; ++kb, ++it) {
       const int s = it % C::STAGES;
       uint8_t* dst = R.kv_s + s * C::STAGE_BYTES + (is_k ? 0 : C::K_BYTES);
@@ -272,6 +275,11 @@ __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bo
       mbar_arrive_expect_tx(&full[s], bytes);
       for (int p = 0; p < panels; ++p)
         tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, kb * BLK_N, bh);
+      // L2 requests for the blocks past the ring, after the first block's
+      // load so that they do not delay it
+      if (kb == 0)
+        for (int pk = C::STAGES; pk < C::STAGES + PREFETCH && pk < u.nmax; ++pk)
+          for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, pk * BLK_N, bh);
       const int ahead = kb + C::STAGES + PREFETCH;
       if (ahead < u.nmax)
         for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, ahead * BLK_N, bh);
@@ -279,7 +287,9 @@ __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bo
     ++ui;
   }
   if (gave_up) {  // let this thread's loads land before the CTA exits
-    if (is_k && q_last >= 0) drain(R.q_full, q_last & 1);
+    if (is_k)
+      for (int k = q_last - C::Q_BUFS + 1; k <= q_last; ++k)
+        if (k >= 0) drain(R.q_full + k % C::Q_BUFS, (k / C::Q_BUFS) & 1);
     for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
       drain(&full[k % C::STAGES], (k / C::STAGES) & 1);
   }
@@ -707,9 +717,14 @@ struct SpCfg {
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
   // barriers (up to 64 x 8 B), then the exchange [2 tiles][2 halves][2 slots][128]
   static constexpr int EXTRA_SP = 512 + 2 * 2 * 2 * 128 * 4;
-  static constexpr int BUDGET = 227 * 1024 - 2 * Q_TILE_BYTES - 1024 - EXTRA_SP;
+  // a second pair of Q tiles (the next unit's, loaded while the current one
+  // runs) where it leaves the ring at four stages
+  static constexpr int Q_BUFS =
+      (227 * 1024 - 4 * Q_TILE_BYTES - 1024 - EXTRA_SP) / STAGE_BYTES >= 4 ? 2 : 1;
+  static constexpr int BUDGET = 227 * 1024 - 2 * Q_BUFS * Q_TILE_BYTES - 1024 - EXTRA_SP;
   static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 4 ? 4 : (BUDGET / STAGE_BYTES);
-  static constexpr int SMEM = 2 * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA_SP;
+  static constexpr int SMEM =
+      2 * Q_BUFS * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA_SP;
   // TMEM columns of tile t: S at 128 t, P at 256 + 64 t, z at 384 + 64 t
   static constexpr uint32_t S_COL = 0, P_COL = 256, O_COL = 384;
   static_assert(STAGES >= 2, "shared memory");
@@ -728,11 +743,11 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* q_s = smem;
-  uint8_t* kv_s = smem + 2 * C::Q_TILE_BYTES;
+  uint8_t* kv_s = smem + 2 * C::Q_BUFS * C::Q_TILE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + C::STAGES * C::STAGE_BYTES);
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = q_full + 1;
-  uint64_t* k_full = q_empty + 1;           // [STAGES]
+  uint64_t* q_full = bars;                  // [Q_BUFS]
+  uint64_t* q_empty = q_full + C::Q_BUFS;   // [Q_BUFS]
+  uint64_t* k_full = q_empty + C::Q_BUFS;   // [STAGES]
   uint64_t* v_full = k_full + C::STAGES;    // [STAGES]
   uint64_t* k_empty = v_full + C::STAGES;   // [STAGES]
   uint64_t* v_empty = k_empty + C::STAGES;  // [STAGES]
@@ -746,8 +761,10 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   float* xchg = reinterpret_cast<float*>(bars + 64);
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 2);
+    for (int b = 0; b < C::Q_BUFS; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 2);
+    }
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
@@ -788,7 +805,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       const uint32_t idesc_qk =
           idesc_bf16_f32(BLK_M, BLK_N, 0, 0) | (P.negate ? (1u << 13) : 0u);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BLK_M, DV, 0, 1);
-      const uint64_t qd = sdesc_sw128(smem_u32(q_s + t * C::Q_TILE_BYTES), 16, 1024);
+      const uint64_t qd0 = sdesc_sw128(smem_u32(q_s + t * C::Q_TILE_BYTES), 16, 1024);
+      uint64_t qd = qd0;  // the current unit's Q buffer
       const uint64_t k_desc = sdesc_sw128(smem_u32(kv_s), 16, 1024);
       const uint64_t v_desc = sdesc_sw128(smem_u32(kv_s + C::K_BYTES), 16384, 1024);
       constexpr uint64_t STAGE_D = C::STAGE_BYTES >> 4;
@@ -828,7 +846,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         const Unit u = unit_at(P, idx);
         if (u.nmax == 0) continue;
         const int nbt = t ? u.nb1 : u.nb0;
-        if (!mbar_wait(q_full, ui & 1, w)) {
+        const int qb = ui % C::Q_BUFS;
+        qd = qd0 + (uint64_t)((qb * 2 * C::Q_TILE_BYTES) >> 4);
+        if (!mbar_wait(q_full + qb, (ui / C::Q_BUFS) & 1, w)) {
           ok = false;
           break;
         }
@@ -842,7 +862,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           issue_s(base);
           ++cs;
           inflight = true;
-          if (nbt == 1) umma_commit(q_empty);  // the unit's last S is issued
+          if (nbt == 1) umma_commit(q_empty + qb);  // the unit's last S is issued
           for (int kb = 0; kb < nbt; ++kb, ++c) {
             const uint32_t r = base + kb;
             if (kb + 1 < nbt) {
@@ -854,7 +874,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
               tc_fence_after();
               issue_s(r + 1);
               ++cs;
-              if (kb + 2 == nbt) umma_commit(q_empty);
+              if (kb + 2 == nbt) umma_commit(q_empty + qb);
             }
             if (!mbar_wait(&v_full[r % C::STAGES], (r / C::STAGES) & 1, w) ||
                 !mbar_wait(&p_full[t], c & 1, w) ||
@@ -868,7 +888,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           if (!ok) break;
           ++act;
         } else {
-          mbar_arrive(q_empty);  // this tile has no rows in the unit: no S reads Q
+          mbar_arrive(q_empty + qb);  // this tile has no rows in the unit: no S reads Q
         }
         for (int k2 = nbt; k2 < u.nmax && ok; ++k2) {
           const uint32_t r = base + k2;
