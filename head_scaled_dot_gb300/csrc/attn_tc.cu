@@ -199,14 +199,17 @@ __device__ __forceinline__ Unit unit_at(const AttnTcParams& P, int idx) {
   return u;
 }
 
-// The i-th unit of this CTA, or -1 past the end. Round i hands units
+// The i-th unit of CTA c of G, or -1 past the end. Round i hands units
 // [i G, i G + G) to the G CTAs, in reverse CTA order on odd rounds, so a CTA
 // that drew a heavy causal pair in one round draws a light one in the next.
 // With as many CTAs as units every CTA takes exactly its own unit.
-__device__ __forceinline__ int unit_index(const AttnTcParams& P, int i) {
-  const int G = gridDim.x, c = blockIdx.x;
+__host__ __device__ inline int unit_index_of(const AttnTcParams& P, int G, int c, int i) {
   const int idx = i * G + ((i & 1) ? G - 1 - c : c);
   return idx < P.units ? idx : -1;
+}
+
+__device__ __forceinline__ int unit_index(const AttnTcParams& P, int i) {
+  return unit_index_of(P, gridDim.x, blockIdx.x, i);
 }
 
 // The shared-memory ring and barriers a TMA producer thread fills.
@@ -1122,9 +1125,9 @@ double persistent_makespan(const AttnTcParams& P, int G, double sr) {
   for (int c = 0; c < G; ++c) {
     double t = 0;
     for (int i = 0;; ++i) {
-      const long long idx = (long long)i * G + ((i & 1) ? G - 1 - c : c);
-      if (idx >= P.units) break;
-      t += unit_cost_host(P, (int)idx, sr) + PERSIST_FIXED;
+      const int idx = unit_index_of(P, G, c, i);
+      if (idx < 0) break;
+      t += unit_cost_host(P, idx, sr) + PERSIST_FIXED;
     }
     worst = t > worst ? t : worst;
   }
@@ -1145,9 +1148,8 @@ double per_unit_makespan(const AttnTcParams& P, int G, double sr) {
 }
 
 // Picks one CTA per unit or a persistent grid (and the unit order) for the
-// shorter estimated time; returns the grid size.
-int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh) {
-  const int G = num_sms();
+// shorter estimated time on G SMs; returns the grid size.
+int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh, int G) {
   const int pairs = P.npair * P.nbh;
   const double sr = 1.0 + 4.0 * (d_h + d_vh) / 1600.0;
   P.pi_major = 0;
@@ -1225,7 +1227,56 @@ mha_status launch_sp(const AttnTcParams& P, int grid, cudaStream_t s) {
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
+// The units of an attention call: tile pairs of every (batch item, head),
+// with the lengths the masks use. Host only, no device work.
+mha_status set_units(AttnTcParams& P, const AttnArgs& a) {
+  P.n_q = a.n_q;
+  P.n_k = a.n_k;
+  P.h = a.h;
+  P.npair = (a.n_q + 2 * BLK_M - 1) / (2 * BLK_M);
+  const long long units = (long long)P.npair * a.h * a.B;
+  if (units > (1ll << 29)) return MHA_ERR_UNSUPPORTED;
+  P.units = P.pair_units = (int)units;
+  P.nbh = a.h * a.B;
+  P.causal = a.causal;
+  P.padding = a.padding;
+  P.pad_queries = a.pad_queries;
+  for (int b = 0; b < MHA_MAX_PADDED_BATCH; ++b)
+    P.valid_len[b] = (a.padding && b < a.B) ? a.valid_len_host[b] : a.n_k;
+  return MHA_OK;
+}
+
 }  // namespace
+
+mha_status attention_tc_plan(const AttnArgs& a, int num_sms, int* grid, int32_t* records,
+                             size_t max_records, size_t* n_records) {
+  AttnTcParams P;
+  memset(&P, 0, sizeof(P));
+  const mha_status st = set_units(P, a);
+  if (st != MHA_OK) return st;
+  const int G = choose_schedule(P, a.B, a.d_h, a.d_vh, num_sms);
+  *grid = G;
+  size_t n = 0;
+  for (int c = 0; c < G; ++c)
+    for (int i = 0;; ++i) {
+      const int idx = unit_index_of(P, G, c, i);
+      if (idx < 0) break;
+      if (records && n < max_records) {
+        int pi, bh, tile;
+        bool pair;
+        unit_coords(P, idx, pi, bh, tile, pair);
+        int32_t* r = records + 5 * n;
+        r[0] = c;
+        r[1] = bh / P.h;
+        r[2] = bh % P.h;
+        r[3] = pi * 2 * BLK_M + tile * BLK_M;
+        r[4] = pair ? 2 : 1;
+      }
+      ++n;
+    }
+  *n_records = n;
+  return MHA_OK;
+}
 
 mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
   AttnTcParams P;
@@ -1243,31 +1294,20 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
       !make_tmap_bf16(&P.vmap, a.V, 3, vd, vs, box, true))
     return MHA_ERR_CUDA;
   P.Z = a.Z;
-  P.n_q = a.n_q;
-  P.n_k = a.n_k;
-  P.h = a.h;
-  P.npair = (a.n_q + 2 * BLK_M - 1) / (2 * BLK_M);
-  const long long units = (long long)P.npair * a.h * a.B;
-  if (units > (1ll << 29)) return MHA_ERR_UNSUPPORTED;
-  P.units = P.pair_units = (int)units;
-  P.nbh = a.h * a.B;
+  const mha_status st = set_units(P, a);
+  if (st != MHA_OK) return st;
   // |c| log2(e), kept at 1e-30 or above so that a masked score (-inf) stays
   // -inf after scaling; for c = 0 (or |c| below that) every allowed score
   // scales to within 1e-26 of 0 and gets weight 2^0 = 1: the uniform
   // distribution over the allowed keys, as softmax of all-zero scores
   P.cl2 = fmaxf(fabsf(a.c) * 1.4426950408889634f, 1e-30f);
   P.negate = a.c < 0.f;
-  P.causal = a.causal;
-  P.padding = a.padding;
-  P.pad_queries = a.pad_queries;
   P.err = a.err;
   P.limit_ns = wait_limit_ns();
-  for (int b = 0; b < MHA_MAX_PADDED_BATCH; ++b)
-    P.valid_len[b] = (a.padding && b < a.B) ? a.valid_len_host[b] : a.n_k;
   for (int i = 0; i < MHA_MAX_GATED_HEADS; ++i)
     P.head_gate[i] = (a.head_gate_host && i < a.h) ? a.head_gate_host[i] : 1.f;
   // one CTA per unit, or one persistent CTA per SM walking its share
-  const int grid = choose_schedule(P, a.B, a.d_h, a.d_vh);
+  const int grid = choose_schedule(P, a.B, a.d_h, a.d_vh, num_sms());
   // d_vh = 64: S, P and z fit in separate TMEM columns
   if (a.d_h == 64 && a.d_vh == 64) return launch_sp<64>(P, grid, s);
   if (a.d_h == 128 && a.d_vh == 128) return launch<128, 128>(P, grid, s);

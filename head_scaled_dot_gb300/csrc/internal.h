@@ -85,6 +85,12 @@ mha_status attention_simt(const AttnArgs& a, mha_dtype dt, cudaStream_t s);
 // Tensor-core kernels (bf16).
 mha_status gemm_tc(const GemmProblem* probs, int nprob, int32_t* err, cudaStream_t s);
 mha_status attention_tc(const AttnArgs& a, cudaStream_t s);
+// The schedule attention_tc would launch on a GPU with num_sms SMs: the grid
+// size and, CTA by CTA in processing order, one record {cta, b, head, q0,
+// ntiles} per unit (query rows [q0, q0 + 128 ntiles) of one head), at most
+// max_records of them written; *n_records = all units. Host only.
+mha_status attention_tc_plan(const AttnArgs& a, int num_sms, int* grid, int32_t* records,
+                             size_t max_records, size_t* n_records);
 
 // TMA descriptors (cuTensorMapEncodeTiled through the runtime's driver entry
 // point). dims/strides innermost first; strides in bytes for dims 1..rank-1.

@@ -464,6 +464,36 @@ mha_status mha_selftest_wait_timeout(int32_t* dev_error, uint64_t limit_ns, void
   return selftest_wait(dev_error, limit_ns, static_cast<cudaStream_t>(stream));
 }
 
+mha_status mha_attention_plan(int B, int n_q, int n_k, int h, int d_h, int d_vh,
+                              mha_mask_kind mask, const int32_t* valid_len, int self_attention,
+                              int num_sms, int32_t* grid, int32_t* records, size_t max_records,
+                              size_t* n_records) {
+  if (!grid || !n_records || num_sms < 1) return MHA_ERR_INVALID_ARG;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
+    return MHA_ERR_INVALID_ARG;
+  if (!mask_ok(mask)) return MHA_ERR_INVALID_ARG;
+  if (has_causal(mask) && n_q != n_k) return MHA_ERR_INVALID_ARG;
+  if (self_attention && n_q != n_k) return MHA_ERR_INVALID_ARG;
+  const mha_status st = check_valid_len(mask, valid_len, B, n_k);
+  if (st != MHA_OK) return st;
+  if (!tc_head_dims(d_h, d_vh)) return MHA_ERR_UNSUPPORTED;
+  AttnArgs a{};
+  a.B = B;
+  a.n_q = n_q;
+  a.n_k = n_k;
+  a.h = h;
+  a.d_h = d_h;
+  a.d_vh = d_vh;
+  a.causal = has_causal(mask);
+  a.padding = has_padding(mask);
+  a.pad_queries = has_padding(mask) && self_attention;
+  a.valid_len_host = valid_len;
+  int g = 0;
+  const mha_status ps = attention_tc_plan(a, num_sms, &g, records, max_records, n_records);
+  *grid = g;
+  return ps;
+}
+
 uint64_t mha_kernel_launch_count(void) { return g_launches.load(); }
 
 const char* mha_version(void) { return "head_scaled_dot_gb300 0.1 (sm_103a)"; }

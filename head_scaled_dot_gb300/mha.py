@@ -34,7 +34,7 @@ EXPORTS = (
     "mha_output_projection", "mha_get_device_error", "mha_status_string",
     "mha_selftest_wait_timeout", "mha_kernel_launch_count", "mha_version",
     "mha_forward_no_alloc", "mha_forward_general", "mha_decode_workspace_size",
-    "mha_attention_decode",
+    "mha_attention_decode", "mha_attention_plan",
 )
 
 _lib = None
@@ -86,6 +86,8 @@ def load(path=LIB_PATH):
     lib.mha_kernel_launch_count.argtypes = []
     lib.mha_version.restype = ctypes.c_char_p
     lib.mha_version.argtypes = []
+    lib.mha_attention_plan.restype = I
+    lib.mha_attention_plan.argtypes = [I] * 6 + [I, P, I, I, P, P, S, P]
     _lib = lib
     return lib
 
@@ -134,6 +136,25 @@ def workspace_layout(B, n_q, n_k, h, d_h, d_vh, dtype):
     _check(load().mha_workspace_layout(B, n_q, n_k, h, d_h, d_vh, DTYPES[dtype], off),
            "mha_workspace_layout")
     return dict(zip(("err", "q", "k", "v", "z", "total"), [int(x) for x in off]))
+
+
+def attention_plan(B, n_q, n_k, h, d_h, d_vh, mask="none", valid_len=None,
+                   self_attention=True, num_sms=152):
+    """The tensor-core attention schedule for a GPU with num_sms SMs (host
+    only): (grid, records), records an int32 array of rows (cta, b, head, q0,
+    ntiles), CTA by CTA in processing order."""
+    import numpy as np
+    lib = load()
+    lens_arg, keep = _lens(valid_len, B)
+    grid = ctypes.c_int32()
+    n = ctypes.c_size_t()
+    args = (B, n_q, n_k, h, d_h, d_vh, MASKS[mask], lens_arg, 1 if self_attention else 0,
+            num_sms, ctypes.byref(grid))
+    _check(lib.mha_attention_plan(*args, None, 0, ctypes.byref(n)), "mha_attention_plan")
+    rec = (ctypes.c_int32 * (5 * max(1, n.value)))()
+    _check(lib.mha_attention_plan(*args, rec, n.value, ctypes.byref(n)), "mha_attention_plan")
+    del keep
+    return grid.value, np.ctypeslib.as_array(rec).reshape(-1, 5)[:n.value].copy()
 
 
 def launch_count():

@@ -224,6 +224,29 @@ MHA_API mha_status mha_attention(const void* Q, const void* K, const void* V, vo
                          void* stream);
 
 /*
+ * The schedule mha_attention uses for bf16 heads of 64 or 128 (the
+ * tensor-core kernels), computed on the host for a GPU with num_sms SMs;
+ * it launches nothing and needs no GPU. A unit is one 128-row query tile or
+ * a pair of them, of one (batch item, head); each CTA of the grid takes its
+ * units in order. Outputs:
+ *   *grid        CTAs the launch would use (num_sms for the persistent
+ *                schedule, the number of units for one CTA per unit)
+ *   records      HOST int32 array of 5 * max_records (may be NULL): for each
+ *                unit, CTA by CTA in processing order, {cta, b, head, q0,
+ *                ntiles}: query rows [q0, q0 + 128 ntiles) of head `head` of
+ *                batch item b (rows at or past n_q do not exist); at most
+ *                max_records records are written
+ *   *n_records   the number of units (records needed)
+ * Arguments as for mha_attention; MHA_ERR_INVALID_ARG on a NULL grid or
+ * n_records, num_sms < 1 or an invalid size or mask, MHA_ERR_EMPTY_ROW on a
+ * bad valid length, MHA_ERR_UNSUPPORTED for other head sizes.
+ */
+MHA_API mha_status mha_attention_plan(int B, int n_q, int n_k, int h, int d_h, int d_vh,
+                              mha_mask_kind mask, const int32_t* valid_len,
+                              int self_attention, int num_sms, int32_t* grid,
+                              int32_t* records, size_t max_records, size_t* n_records);
+
+/*
  * Step 3: Y (B*n_q, d_o) = Z (B*n_q, h*d_vh) W_O (h*d_vh, d_o)
  * ("The Complete Multi-Head Operation": Y = Z W_O).
  */
