@@ -420,6 +420,15 @@ def cpu_baseline(w, inp, lens, budget_s=12.0):
                       "fp64 numpy, %.1f s" % (done, w.name, done / len(units), len(units), secs)}
 
 
+def workload_config(w, lens):
+    """The keys naming a workload in the JSON line (both arms)."""
+    from head_scaled_dot_gb300 import workcount
+    return {"workload": w.name, "B": w.B, "n_q": w.n_q, "n_k": w.n_k, "d_model": w.d_model,
+            "h": w.h, "d_h": w.d_h, "d_vh": w.d_vh, "d_o": w.d_o, "mask": w.mask,
+            "cross": w.cross, "seed": w.seed, "valid_len": lens,
+            "gflop_per_step": workcount.flops(w, lens)["total"] / 1e9}
+
+
 def run_reference(args):
     import torch
     rank, world, _ = dist_setup(args.gpus)
@@ -443,7 +452,8 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "step": "one (batch item, head) unit per step"},
+            "config": dict(workload_config(w, lens),
+                           step="one (batch item, head) unit of the workload per step"),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": "one (batch item, head) unit of %s per step, %d steps"
                                        % (w.name, args.steps)},
@@ -519,14 +529,11 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "n_q": w.n_q, "n_k": w.n_k,
-                   "d_model": w.d_model, "h": w.h, "d_h": w.d_h, "d_vh": w.d_vh, "d_o": w.d_o,
-                   "mask": w.mask, "cross": w.cross, "seed": w.seed,
-                   "valid_len": res["lens"], "l2": "flushed between timed steps (512 MiB write)",
-                   "clocks": "nvidia-smi every 200 ms over a 1 s window of identical untimed "
-                             "steps that ends where the timed steps begin",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "gflop_per_step": fl / 1e9},
+        "config": dict(workload_config(w, res["lens"]),
+                       l2="flushed between timed steps (512 MiB write)",
+                       clocks="nvidia-smi every 200 ms over a 1 s window of identical untimed "
+                              "steps that ends where the timed steps begin",
+                       parallelism="replicas" if world > 1 else "single GPU"),
         "frac_of_bf16_peak": value / world / pk["bf16_tflops"],
         "roofline": roof,
         "kernels": krows,

@@ -51,3 +51,10 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    # the same workload keys as the GPU arm's line, the default workload
+    import bench
+    from head_scaled_dot_gb300 import workloads
+    w = workloads.WORKLOADS[1]
+    for k, v in bench.workload_config(w, None).items():
+        assert d["config"][k] == v, k
+    assert d["metric"] == bench.METRIC and d["higher_is_better"] is True
