@@ -66,6 +66,26 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# FP32 lanes per SM (four schedulers x 32) and flop per FMA: the peak of the
+# CUDA-core kernels is SMs x 128 x 2 x the maximum SM clock.
+FP32_LANES_PER_SM = 128
+
+
+def alu_peak_tflops(dev, sm_max_mhz):
+    """fp32 FMA peak of the device at the given SM clock, in TFLOP/s."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return sms * FP32_LANES_PER_SM * 2 * sm_max_mhz * 1e6 / 1e12
+
+
+def sm_max_mhz():
+    """Maximum SM clock: the measured-peaks record, else the GB300 maximum."""
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["sm_max_mhz"])
+    except Exception:
+        return 2070.0
+
+
 def dist_setup(n):
     import torch
     import torch.distributed as dist
@@ -496,8 +516,10 @@ def run_ours(args):
     roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "peak_kind": pk_kind + " burst",
             "traffic": stored_traffic(dom, w.name)}
-    if w.dtype == "f32":
-        roof["bound"] = "alu"
+    if w.dtype == "f32":  # every kernel of the fp32 path runs on the CUDA cores
+        alu = alu_peak_tflops(dev, sm_max_mhz())
+        roof.update(bound="alu", peak=alu, frac=ach / alu,
+                    peak_kind="derived: SMs x 128 FP32 lanes x 2 flop x max SM clock")
     others = {}
     if not args.no_others and rank == 0:
         for j, wj in enumerate(workloads.WORKLOADS):
@@ -511,6 +533,23 @@ def run_ours(args):
                                "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
                                "kernels": kr}
             del r
+        # a general head size: attention on the CUDA cores, against the fp32 FMA peak
+        gw = workloads.GENERAL_DIMS
+        r = measure_workload(gw, max(3, args.steps // 2), 3, dev, 1, e2e=False,
+                             sample_clocks=False)
+        kr = kernel_rows(r, pk)
+        alu = alu_peak_tflops(dev, sm_max_mhz())
+        others[gw.name] = {"tflops": r["flops"]["total"] * len(r["per"]["step"])
+                           / (r["total_ms"] * 1e-3) / 1e12,
+                           "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
+                           "kernels": kr,
+                           "roofline": {"kernel": "attention (CUDA cores)", "bound": "alu",
+                                        "achieved": kr["attention"]["tflops"], "peak": alu,
+                                        "unit": "TFLOP/s",
+                                        "frac": kr["attention"]["tflops"] / alu,
+                                        "peak_kind": "derived: SMs x 128 FP32 lanes x 2 flop "
+                                                     "x max SM clock"}}
+        del r
         dw = workloads.DECODE
         others[dw.name] = measure_decode(dw, max(3, args.steps), 3, dev, pk)
     cpu = None

@@ -61,16 +61,16 @@ def sample_rows(w, L, rng, n=24):
     return sorted(c for c in cand if 0 <= c < hi)
 
 
-@pytest.mark.parametrize("idx", [2, 3, 4])
+@pytest.mark.parametrize("idx", [2, 3, 4, "general_dims"])
 def test_workload_sampled_rows(idx):
-    w = workloads.WORKLOADS[idx]
+    w = workloads.GENERAL_DIMS if idx == "general_dims" else workloads.WORKLOADS[idx]
     inp = workloads.make_inputs(w)
     got = f64(run(w, inp))
     assert np.isfinite(got).all()
     rows_ok = computed_rows(w, inp)
     assert np.all(got[~rows_ok] == 0.0)
     lens = lens_list(inp)
-    rng = np.random.default_rng(idx)
+    rng = np.random.default_rng(w.seed)
     batches = range(w.B) if w.B <= 4 else sorted(set([0, w.B - 1] + rng.integers(0, w.B, 2).tolist()))
     worst = 0.0
     for b in batches:
