@@ -82,6 +82,7 @@ struct AttnTcParams {
   CUtensorMap vmap;  // V: dims {d_vh, n_k, B*h}, box {64, 128, 1}
   void* Z;
   int n_q, n_k, h;
+  int dv;            // d_vh: columns of z written per head (DV of the kernel or fewer)
   int npair;         // 256-row query tile pairs per (batch item, head)
   int units;         // units of work: pair_units pairs, then single tiles
   int pair_units;    // the first pair_units units are tile pairs; each later
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   using C = ACfg<DQK, DV>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   __nv_bfloat16* Zg = static_cast<__nv_bfloat16*>(P.Z);
-  const long long zrow_stride = (long long)P.h * DV;
+  const long long zrow_stride = (long long)P.h * P.dv;  // d_vh <= DV columns per head
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -526,7 +527,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int idx = unit_index(P, i);
       if (idx < 0) break;
       const Unit u = unit_at(P, idx);
-      const long long zbase = (long long)u.b * P.n_q * zrow_stride + (long long)u.head * DV;
+      const long long zbase = (long long)u.b * P.n_q * zrow_stride + (long long)u.head * P.dv;
       float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
       for (int kb = 0; kb < u.nmax; ++kb) {
 #pragma unroll
@@ -648,7 +649,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (q < P.n_q) {
 #pragma unroll
             for (int j = 0; j < DV / 16; ++j)
-              reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
+              if (half * (DV / 2) + 8 * j < P.dv)
+                reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
           }
           continue;
         }
@@ -677,9 +679,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                              __uint_as_float(o[2 * j + 1]) * inv)
                                : 0u;
             uint4* dst = reinterpret_cast<uint4*>(zrow + 32 * cb);
+            // columns past d_vh (V was read as zeros there) are not written
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              if (half * (DV / 2) + 32 * cb + 8 * j < P.dv)
+                dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           }
         }
         tc_fence_before();
@@ -1294,6 +1298,7 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
       !make_tmap_bf16(&P.vmap, a.V, 3, vd, vs, box, true))
     return MHA_ERR_CUDA;
   P.Z = a.Z;
+  P.dv = a.d_vh;
   const mha_status st = set_units(P, a);
   if (st != MHA_OK) return st;
   // |c| log2(e), kept at 1e-30 or above so that a masked score (-inf) stays
@@ -1308,12 +1313,16 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
     P.head_gate[i] = (a.head_gate_host && i < a.h) ? a.head_gate_host[i] : 1.f;
   // one CTA per unit, or one persistent CTA per SM walking its share
   const int grid = choose_schedule(P, a.B, a.d_h, a.d_vh, num_sms());
-  // d_vh = 64: S, P and z fit in separate TMEM columns
-  if (a.d_h == 64 && a.d_vh == 64) return launch_sp<64>(P, grid, s);
-  if (a.d_h == 128 && a.d_vh == 128) return launch<128, 128>(P, grid, s);
-  if (a.d_h == 64 && a.d_vh == 128) return launch<64, 128>(P, grid, s);
-  if (a.d_h == 128 && a.d_vh == 64) return launch_sp<128>(P, grid, s);
-  return MHA_ERR_UNSUPPORTED;
+  // Head sizes between 64 and 128 run as 128: the 64-wide panels past d_h
+  // (past d_vh) are read as zeros (TMA fill past the tensor's extent), so
+  // the padded dot products are exact and z's extra columns stay 0 and are
+  // not written. d_vh = 64: S, P and z fit in separate TMEM columns.
+  if (a.d_h < 64 || a.d_h > 128 || a.d_vh < 64 || a.d_vh > 128) return MHA_ERR_UNSUPPORTED;
+  const bool q64 = a.d_h == 64, v64 = a.d_vh == 64;
+  if (q64 && v64) return launch_sp<64>(P, grid, s);
+  if (!q64 && !v64) return launch<128, 128>(P, grid, s);
+  if (q64) return launch<64, 128>(P, grid, s);
+  return launch_sp<128>(P, grid, s);
 }
 
 }  // namespace mha

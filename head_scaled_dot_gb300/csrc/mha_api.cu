@@ -134,8 +134,9 @@ Layout layout(int B, int n_q, int n_k, int h, int d_h, int d_vh, mha_dtype dt) {
   return L;
 }
 
-// Head sizes every path handles: 1 .. MAX_HEAD_DIM. bf16 heads of 64 or 128
-// run on the tensor cores, other sizes on the CUDA-core kernel.
+// Head sizes every path handles: 1 .. MAX_HEAD_DIM. bf16 heads of 64..128
+// (multiples of 8) run on the tensor cores, other sizes on the CUDA-core
+// kernel.
 constexpr int MAX_HEAD_DIM = 256;
 
 mha_status check_head_dims(int d_h, int d_vh, mha_dtype dt) {
@@ -144,8 +145,12 @@ mha_status check_head_dims(int d_h, int d_vh, mha_dtype dt) {
   return MHA_OK;
 }
 
+// Head sizes the tensor-core attention kernels take: 64, or 72..128 run in
+// the 128-wide kernels (multiples of 8, as their tensor maps need 16-byte
+// strides).
 bool tc_head_dims(int d_h, int d_vh) {
-  return (d_h == 64 || d_h == 128) && (d_vh == 64 || d_vh == 128);
+  auto ok = [](int d) { return d >= 64 && d <= 128 && d % 8 == 0; };
+  return ok(d_h) && ok(d_vh);
 }
 
 // Elements beyond 2^31 per tensor are not addressed by every index path.

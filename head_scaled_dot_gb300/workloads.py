@@ -64,8 +64,8 @@ WORKLOADS = [
 
 
 # A general head size (d_h = 96, neither 64 nor 128): the attention step runs
-# on the CUDA cores in fp32 arithmetic on bf16 data. Measured beside the five
-# above (not a benchmark headline); seed 6.
+# in the 128-wide tensor-core kernel with the columns past 96 read as zeros.
+# Measured beside the five above (not a benchmark headline); seed 6.
 GENERAL_DIMS = _w("self_bf16_B4_T1024_d768_h8_dh96_none", 4, 1024, 768, 8, 96, "none", "bf16",
                   1 / math.sqrt(96), 6)
 

@@ -135,7 +135,9 @@ MHA_API mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h,
  *                                aligned; its contents on entry do not matter
  *
  * Head sizes d_h, d_vh from 1 to 256 (MHA_ERR_UNSUPPORTED otherwise); bf16
- * heads of 64 or 128 run on the tensor cores, other sizes on CUDA cores.
+ * heads with d_h and d_vh in 64..128 and multiples of 8 run on the tensor
+ * cores (sizes above 64 in the 128-wide kernels, the columns past d_h or d_vh
+ * read as zeros), other sizes on CUDA cores.
  * bf16 also needs d_model, d_h, d_vh and d_o to be multiples of 8.
  * Enqueues a 4-byte memset of the error word and three kernels. Everything
  * it enqueues is stream-ordered, so the call can be captured in a CUDA graph
@@ -177,8 +179,9 @@ MHA_API mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_
  *                                any d_model: the intermediates do not depend
  *                                on the input widths)
  *
- * Head sizes d_h, d_vh from 1 to 256; bf16 heads of 64 or 128 run on the
- * tensor cores, other sizes on CUDA cores. bf16 also needs d_q, d_k, d_v,
+ * Head sizes d_h, d_vh from 1 to 256; bf16 heads with d_h and d_vh in 64..128
+ * run on the tensor cores (as for mha_forward), other sizes on CUDA cores.
+ * bf16 also needs d_q, d_k, d_v,
  * d_h, d_vh and d_o to be multiples of 8 and 16-byte aligned pointers
  * (MHA_ERR_UNSUPPORTED otherwise). Other errors as for mha_forward.
  * mha_forward is this call with X_k = X_v = X_kv (or X_q) and
@@ -224,8 +227,9 @@ MHA_API mha_status mha_attention(const void* Q, const void* K, const void* V, vo
                          void* stream);
 
 /*
- * The schedule mha_attention uses for bf16 heads of 64 or 128 (the
- * tensor-core kernels), computed on the host for a GPU with num_sms SMs;
+ * The schedule mha_attention uses for bf16 heads on the tensor cores (d_h
+ * and d_vh in 64..128, multiples of 8), computed on the host for a GPU with
+ * num_sms SMs;
  * it launches nothing and needs no GPU. A unit is one 128-row query tile or
  * a pair of them, of one (batch item, head); each CTA of the grid takes its
  * units in order. Outputs:

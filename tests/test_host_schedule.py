@@ -78,7 +78,7 @@ def test_every_tile_exactly_once(mask, sms):
         self_attention = bool(rng.integers(2)) or "causal" in mask
         n_q = n
         n_k = n if self_attention else int(rng.choice(SIZES))
-        d = [(64, 64), (128, 128), (64, 128), (128, 64)][trial % 4]
+        d = [(64, 64), (128, 128), (64, 128), (128, 64), (96, 72)][trial % 5]
         lens = [int(x) for x in rng.integers(1, n_k + 1, B)] if "padding" in mask else None
         check_plan(B, n_q, n_k, h, d, mask, lens, self_attention, sms)
 
@@ -99,7 +99,10 @@ def test_plan_rejects_what_attention_rejects():
         return 0
     assert status(2, 256, 256, 4, 64, 64, num_sms=0) == 1            # INVALID_ARG
     assert status(2, 256, 128, 4, 64, 64, "causal", self_attention=False) == 1
-    assert status(2, 256, 256, 4, 96, 64) == 2                        # UNSUPPORTED head size
+    assert status(2, 256, 256, 4, 96, 64) == 0                        # 96 runs as 128
+    assert status(2, 256, 256, 4, 48, 64) == 2                        # UNSUPPORTED head sizes
+    assert status(2, 256, 256, 4, 64, 100) == 2
+    assert status(2, 256, 256, 4, 136, 64) == 2
     assert status(2, 256, 256, 4, 64, 64, "padding", [0, 10]) == 3    # EMPTY_ROW
     assert status(2, 256, 256, 4, 64, 64, "padding", [10, 257]) == 3
     assert status(1025, 8, 8, 1, 64, 64, "padding", [1] * 1025) == 2  # beyond the length table
