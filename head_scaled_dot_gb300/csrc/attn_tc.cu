@@ -9,9 +9,12 @@
 // and writes z / l once per row. The n_q x n_k score matrix only ever exists
 // as one 128 x 128 block per tile, in tensor memory (TMEM).
 //
-// Two kernels share the units, the schedule and the TMA producers:
+// Two kernels share the units, the schedule and the TMA producers. Head sizes
+// d of 72..128 run with DQK or DV = 128: Q, K and V are loaded as 64-wide
+// panels and the columns past d come in as zeros (TMA fill past the tensor's
+// extent), so the dot products are exact and z's extra columns stay 0.
 //
-// attn_tc_kernel<DQK, DV> (d_vh = 128; 384 threads):
+// attn_tc_kernel<DQK, DV> (DV = 128, d_vh of 72..128; 384 threads):
 //   warps 0, 2    TMA producers: warp 0 loads the Q tiles of each unit and the
 //                 K blocks, warp 2 the V blocks, into a STAGES-deep ring (K
 //                 and V freed separately); each also prefetches the blocks a
