@@ -98,7 +98,8 @@ struct AttnTcParams {
   int32_t* err;
   uint64_t limit_ns;
   int valid_len[MHA_MAX_PADDED_BATCH];
-  float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale (1: no gate)
+  int has_gate;                          // head_gate holds h entries (h <= MHA_MAX_GATED_HEADS)
+  float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale, read only when has_gate
 };
 
 // bytes after the K/V ring: barriers (up to 64 x 8 B) and the 2 KB exchange
@@ -668,7 +669,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tc_fence_after();
         const bool computed = q < u.q_end;
-        const float inv = computed ? P.head_gate[u.head] / l_tot : 0.f;
+        const float inv = computed ? (P.has_gate ? P.head_gate[u.head] : 1.f) / l_tot : 0.f;
 #pragma unroll
         for (int cb = 0; cb < DV / 64; ++cb) {
           uint32_t o[32];
@@ -1066,7 +1067,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       }
       tc_fence_after();
       const bool computed = q < u.q_end;
-      const float inv = computed ? P.head_gate[u.head] / l_tot : 0.f;
+      const float inv = computed ? (P.has_gate ? P.head_gate[u.head] : 1.f) / l_tot : 0.f;
       uint32_t o[32];
       tmem_ld32(o_addr + 32 * half, o);
       tmem_wait_ld();
@@ -1205,13 +1206,7 @@ int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh, int G) {
 template <int DQK, int DV>
 mha_status launch(const AttnTcParams& P, int grid, cudaStream_t s) {
   using C = ACfg<DQK, DV>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return MHA_ERR_CUDA;
-    attr = true;
-  }
+  if (!ensure_smem_limit((const void*)attn_tc_kernel<DQK, DV>, C::SMEM)) return MHA_ERR_CUDA;
   const cudaError_t e =
       launch_dependent(attn_tc_kernel<DQK, DV>, dim3(grid), dim3(NTHREADS), C::SMEM, s, P);
   count_launch();
@@ -1221,13 +1216,7 @@ mha_status launch(const AttnTcParams& P, int grid, cudaStream_t s) {
 template <int DQK>
 mha_status launch_sp(const AttnTcParams& P, int grid, cudaStream_t s) {
   using C = SpCfg<DQK>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_tc_sp_kernel<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return MHA_ERR_CUDA;
-    attr = true;
-  }
+  if (!ensure_smem_limit((const void*)attn_tc_sp_kernel<DQK>, C::SMEM)) return MHA_ERR_CUDA;
   const cudaError_t e =
       launch_dependent(attn_tc_sp_kernel<DQK>, dim3(grid), dim3(SP_THREADS), C::SMEM, s, P);
   count_launch();
@@ -1312,8 +1301,11 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
   P.negate = a.c < 0.f;
   P.err = a.err;
   P.limit_ns = wait_limit_ns();
+  // a gate is only ever passed for h <= MHA_MAX_GATED_HEADS (checked by the
+  // caller); without one every head is read with scale 1, for any h
+  P.has_gate = a.head_gate_host != nullptr && a.h <= MHA_MAX_GATED_HEADS;
   for (int i = 0; i < MHA_MAX_GATED_HEADS; ++i)
-    P.head_gate[i] = (a.head_gate_host && i < a.h) ? a.head_gate_host[i] : 1.f;
+    P.head_gate[i] = (P.has_gate && i < a.h) ? a.head_gate_host[i] : 1.f;
   // one CTA per unit, or one persistent CTA per SM walking its share
   const int grid = choose_schedule(P, a.B, a.d_h, a.d_vh, num_sms());
   // Head sizes between 64 and 128 run as 128: the 64-wide panels past d_h

@@ -797,21 +797,10 @@ bool launch_fast(const DecodeParams& P, const dim3& g1, cudaStream_t s) {
 template <int NQ, int D>
 bool launch_stream(const DecodeParams& P, cudaStream_t s) {
   using C = DsCfg<NQ, D>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(decode_stream_kernel<NQ, D>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-      return false;
-    attr = true;
-  }
+  if (!ensure_smem_limit((const void*)decode_stream_kernel<NQ, D>, C::SMEM)) return false;
   // as many CTAs as can be resident at once (shared memory and registers),
-  // asked once
-  static int per_sm = 0;
-  if (per_sm < 1 &&
-      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<NQ, D>,
-                                                     DS_THREADS, C::SMEM) != cudaSuccess ||
-       per_sm < 1))
-    per_sm = 1;
+  // asked once per device
+  const int per_sm = resident_ctas((const void*)decode_stream_kernel<NQ, D>, DS_THREADS, C::SMEM);
   const int cap = num_sms() * per_sm;
   const int grid = P.nitems < cap ? P.nitems : cap;
   decode_stream_kernel<NQ, D><<<grid, DS_THREADS, C::SMEM, s>>>(P);

@@ -24,20 +24,34 @@ struct GemmProblem {
   int M, N, K;
   int rows_per_group, cols_per_group;
   long long s_group_row, s_group_col, s_row;
+  int select;  // rows chosen by the launch's RowSelect (else every row)
 };
 
 static inline GemmProblem plain_problem(const void* A, const void* W, void* out, int M, int N,
                                         int K) {
-  GemmProblem p{A, W, out, M, N, K, M, N, 0, 0, (long long)N};
+  GemmProblem p{A, W, out, M, N, K, M, N, 0, 0, (long long)N, 0};
   return p;
 }
 
 static inline GemmProblem head_split_problem(const void* A, const void* W, void* out, int B,
                                              int T, int h, int d, int K) {
   GemmProblem p{A,  W, out, B * T, h * d, K, T, d, (long long)h * T * d, (long long)T * d,
-                (long long)d};
+                (long long)d, 0};
   return p;
 }
+
+// The rows of a grouped GEMM that matter, for the problems with `select`
+// set: their A rows are B blocks of rows_per_batch rows (one block per batch
+// item), and in block b only the first need[b] rows matter (1 <= need[b] <=
+// rows_per_batch). 128-row output tiles without such a row are not
+// multiplied: they are skipped (their output rows are left as they were), or,
+// with zero_rest (one problem only), written as zeros.
+struct RowSelect {
+  int B;
+  int rows_per_batch;
+  const int32_t* need;  // host, B entries
+  int zero_rest;
+};
 
 // Attention step arguments (Q, K, V head-split; Z concatenated).
 struct AttnArgs {
@@ -73,6 +87,14 @@ struct DecodeArgs {
 size_t decode_workspace_bytes(int B, int n_q, int n_k, int h, int d_vh);
 mha_status attention_decode(const DecodeArgs& a, mha_dtype dt, cudaStream_t s);
 
+// Raises the dynamic shared-memory limit of `kernel` to `bytes` on the
+// current device, once per (device, kernel): the attribute belongs to the
+// device, not to the process. Thread-safe; false on a CUDA error.
+bool ensure_smem_limit(const void* kernel, int bytes);
+// CTAs of `kernel` that fit on one SM of the current device at once (at
+// least 1), asked once per (device, kernel). Thread-safe.
+int resident_ctas(const void* kernel, int threads, int smem_bytes);
+
 // Kernel limit for bounded waits (nanoseconds).
 uint64_t wait_limit_ns();
 void count_launch(int n = 1);
@@ -83,7 +105,12 @@ mha_status gemm_simt(const GemmProblem* probs, int nprob, mha_dtype dt, cudaStre
 mha_status attention_simt(const AttnArgs& a, mha_dtype dt, cudaStream_t s);
 
 // Tensor-core kernels (bf16).
-mha_status gemm_tc(const GemmProblem* probs, int nprob, int32_t* err, cudaStream_t s);
+// Problems with the same A (pointer, M and K) and the same `select` that are
+// next to each other in probs form a group: its tiles run M panel by M panel,
+// each panel through every problem of the group, so the panel of A is read
+// from memory once. sel may be null (every row).
+mha_status gemm_tc(const GemmProblem* probs, int nprob, const RowSelect* sel, int32_t* err,
+                   cudaStream_t s);
 mha_status attention_tc(const AttnArgs& a, cudaStream_t s);
 // The schedule attention_tc would launch on a GPU with num_sms SMs: the grid
 // size and, CTA by CTA in processing order, one record {cta, b, head, q0,

@@ -112,7 +112,8 @@ struct AttnParams {
   float c;
   int causal, padding, pad_queries;
   int valid_len[MHA_MAX_PADDED_BATCH];
-  float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale (1: no gate)
+  int has_gate;                          // head_gate holds h entries (h <= MHA_MAX_GATED_HEADS)
+  float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale, read only when has_gate
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -152,7 +153,8 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_consta
     const int r = e / dq, k = e % dq;
     Qs[e] = (q0 + r < P.n_q) ? to_f(Qg[(long long)(q0 + r) * dq + k]) : 0.f;
   }
-  // Keys this CTA can use: [0, k_end).
+  // Keys this CTA can use: [0, k_end). Rows of K and V at or past L are never
+  // read (loaded as zeros), so they may hold anything.
   int k_end = L;
   if (P.causal) k_end = min(k_end, q0 + AT_ROWS);
 
@@ -169,11 +171,11 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_consta
     __syncthreads();
     for (int e = threadIdx.x; e < AT_KEYS * dq; e += blockDim.x) {
       const int j = e / dq, k = e % dq;
-      Ks[j * (dq + 1) + k] = (k0 + j < P.n_k) ? to_f(Kg[(long long)(k0 + j) * dq + k]) : 0.f;
+      Ks[j * (dq + 1) + k] = (k0 + j < L) ? to_f(Kg[(long long)(k0 + j) * dq + k]) : 0.f;
     }
     for (int e = threadIdx.x; e < AT_KEYS * dv; e += blockDim.x) {
       const int j = e / dv, k = e % dv;
-      Vs[e] = (k0 + j < P.n_k) ? to_f(Vg[(long long)(k0 + j) * dv + k]) : 0.f;
+      Vs[e] = (k0 + j < L) ? to_f(Vg[(long long)(k0 + j) * dv + k]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_consta
     const int q = q0 + warp * 4 + i;
     if (q >= P.n_q) continue;
     const bool computed = q < q_end;
-    const float inv = computed ? P.head_gate[head] / l_run[i] : 0.f;
+    const float inv = computed ? (P.has_gate ? P.head_gate[head] : 1.f) / l_run[i] : 0.f;
     T* zrow = Zg + ((long long)b * P.n_q + q) * (long long)P.h * dv + (long long)head * dv;
 #pragma unroll
     for (int t = 0; t < AT_DMAX / 32; ++t) {
@@ -277,8 +279,9 @@ mha_status attention_simt(const AttnArgs& a, mha_dtype dt, cudaStream_t s) {
   P.pad_queries = a.pad_queries;
   for (int b = 0; b < MHA_MAX_PADDED_BATCH; ++b)
     P.valid_len[b] = (a.padding && b < a.B) ? a.valid_len_host[b] : a.n_k;
+  P.has_gate = a.head_gate_host != nullptr && a.h <= MHA_MAX_GATED_HEADS;
   for (int i = 0; i < MHA_MAX_GATED_HEADS; ++i)
-    P.head_gate[i] = (a.head_gate_host && i < a.h) ? a.head_gate_host[i] : 1.f;
+    P.head_gate[i] = (P.has_gate && i < a.h) ? a.head_gate_host[i] : 1.f;
   const size_t smem =
       sizeof(float) * (AT_ROWS * a.d_h + AT_KEYS * (a.d_h + 1) + AT_KEYS * a.d_vh);
   const dim3 grid((a.n_q + AT_ROWS - 1) / AT_ROWS, a.h, a.B);

@@ -49,3 +49,52 @@ def computed_rows(w, inp):
         for b, L in enumerate(lens):
             rows[b, L:] = False
     return rows
+
+
+def _oracle_head(args):
+    """One (batch item, head) of the oracle's dense attention, for a worker
+    process: (b, i, Q, K, V, c, mask, L, self_attention) -> (b, i, H)."""
+    b, i, Q, K, V, c, mask, L, self_attention = args
+    n_q, n_k = Q.shape[0], K.shape[0]
+    rows = oracle.query_rows_computed(mask, n_q, L, self_attention)
+    allowed = oracle.allowed_keys(mask, n_q, n_k, L)
+    H, _ = oracle.attention(Q, K, V, c, allowed, rows)
+    return b, i, H
+
+
+def oracle_attention_heads(Q, K, V, c, mask, lens, self_attention, workers=None):
+    """Z (B, n_q, h*d_vh) in float64 from head-split Q, K, V (torch tensors of
+    any dtype, on any device): the oracle's dense attention of every
+    (batch item, head), heads concatenated in order.
+
+    The heads run in a pool of spawned worker processes (the elementwise
+    steps of the oracle use one core each); spawn, not fork, because the
+    calling process may already hold a CUDA context."""
+    import multiprocessing as mp
+    import os
+
+    B, h, n_q, _ = Q.shape
+    d_vh = V.shape[3]
+    mk = oracle.MASK_NAMES[mask]
+    Qc, Kc, Vc = Q.cpu(), K.cpu(), V.cpu()
+    jobs = [(b, i, Qc[b, i].double().numpy(), Kc[b, i].double().numpy(),
+             Vc[b, i].double().numpy(), float(c), mk,
+             None if lens is None else int(lens[b]), bool(self_attention))
+            for b in range(B) for i in range(h)]
+    Z = np.zeros((B, n_q, h * d_vh))
+    n = workers or max(1, min(16, os.cpu_count() or 1, len(jobs)))
+    keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in keys}
+    for k in keys:
+        os.environ[k] = "1"  # the workers' BLAS: one thread each
+    try:
+        with mp.get_context("spawn").Pool(n) as pool:
+            for b, i, H in pool.imap_unordered(_oracle_head, jobs):
+                Z[b, :, i * d_vh:(i + 1) * d_vh] = H
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return Z

@@ -13,7 +13,8 @@ import torch
 
 import oracle
 from head_scaled_dot_gb300 import mha, workloads
-from helpers import TOL, computed_rows, f64, lens_list, oracle_forward, rel_err, to_dev
+from helpers import (TOL, computed_rows, f64, lens_list, oracle_attention_heads, oracle_forward,
+                     rel_err, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -81,6 +82,31 @@ def test_workload_sampled_rows(idx):
                                 w.d_vh, w.c, oracle.MASK_NAMES[w.mask], lens, b, rows)
         worst = max(worst, rel_err(got[b, rows], Yr))
     assert worst <= TOL[w.dtype], "rel err %.3e" % worst
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4, "general_dims"])
+def test_workload_full_attention_step(idx):
+    """Every element of Z at full size, in the launch configuration of the
+    benchmark: the attention step on the GPU's own bf16 Q, K, V (from the
+    GPU's projection) against the oracle's dense attention of exactly those
+    values, one (batch item, head) at a time. Padded query rows must be
+    exactly zero; the metric is max|Z - Z_ref| / max|Z_ref| over the computed
+    rows of the whole Z."""
+    w = workloads.GENERAL_DIMS if idx == "general_dims" else workloads.WORKLOADS[idx]
+    inp = workloads.make_inputs(w)
+    t = to_dev(inp)
+    lens = lens_list(inp)
+    Q, K, V = mha.qkv_projection(t["X_q"], t["X_kv"], t["W_Q"], t["W_K"], t["W_V"], w.h, w.d_h,
+                                 w.d_vh)
+    Z = mha.attention(Q, K, V, w.c, w.mask, lens, self_attention=not w.cross)
+    torch.cuda.synchronize()
+    ref = oracle_attention_heads(Q, K, V, w.c, w.mask, lens, not w.cross)
+    got = f64(Z)
+    assert np.isfinite(got).all()
+    rows = computed_rows(w, inp)
+    assert np.all(got[~rows] == 0.0), "padded query rows must be exactly zero"
+    err = rel_err(got[rows], ref[rows])
+    assert err <= TOL[w.dtype], "rel err %.3e > %.0e" % (err, TOL[w.dtype])
 
 
 # ---------------------------------------------------------------------------
@@ -382,3 +408,20 @@ def test_head_gate_zeroes_a_head_like_its_w_o_block(dtype, d):
     # zeroing by gate or by W_O rows: the Z blocks that reach W_O differ only
     # in head 1, whose W_O rows are zero in the second call
     assert rel_err(f64(Yg), f64(Yw)) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("f32", 64)])
+def test_more_heads_than_gate_slots_without_a_gate(dtype, d):
+    """h = 1025 heads (one past the per-head gate table) with no gate: every
+    head, the last ones included, is scaled by exactly 1."""
+    B, h, n = 1, 1025, 130
+    g = torch.Generator().manual_seed(1025 + d)
+    tdt = workloads.torch_dtype(dtype)
+    Q = torch.randn((B, h, n, d), generator=g).to(tdt)
+    K = torch.randn((B, h, n, d), generator=g).to(tdt)
+    V = torch.randn((B, h, n, d), generator=g).to(tdt)
+    c = 1 / math.sqrt(d)
+    Z = mha.attention(Q.cuda(), K.cuda(), V.cuda(), c, "causal", None, self_attention=True)
+    torch.cuda.synchronize()
+    ref = oracle_attention_heads(Q, K, V, c, "causal", None, True)
+    assert rel_err(f64(Z), ref) <= TOL[dtype]
