@@ -44,8 +44,10 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1,
-                    help="workload index (0..4); the JSON line is for this one")
+    ap.add_argument("--config", type=int, default=3,
+                    help="workload index (0..4); the JSON line is for this one (default: 3, "
+                         "the largest: B=2, T=8192, d_model=2048, h=16, d_h=128, causal + "
+                         "padding)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-others", action="store_true",
                     help="skip the per-workload table of the other bf16 workloads")
@@ -221,8 +223,8 @@ def measure_workload(w, steps, warmup, dev, world, e2e=True, sample_clocks=True)
         ev[0].record(stream)
         rc = lib.mha_qkv_projection(P(t["X_q"].data_ptr()), X_kv_p, P(t["W_Q"].data_ptr()),
                                     P(t["W_K"].data_ptr()), P(t["W_V"].data_ptr()), P(Qp), P(Kp),
-                                    P(Vp), B, n_q, n_k, w.d_model, w.h, w.d_h, w.d_vh, DT,
-                                    P(err), sp)
+                                    P(Vp), B, n_q, n_k, w.d_model, w.h, w.d_h, w.d_vh, MK,
+                                    lens_arg, DT, P(err), sp)
         if split:
             ev[1].record(stream)
         rc |= lib.mha_attention(P(Qp), P(Kp), P(Vp), P(Zp), B, n_q, n_k, w.h, w.d_h, w.d_vh,
@@ -230,7 +232,8 @@ def measure_workload(w, steps, warmup, dev, world, e2e=True, sample_clocks=True)
         if split:
             ev[2].record(stream)
         rc |= lib.mha_output_projection(P(Zp), P(t["W_O"].data_ptr()), P(Y.data_ptr()), B, n_q,
-                                        w.h, w.d_vh, w.d_o, DT, P(err), sp)
+                                        w.h, w.d_vh, w.d_o, None if w.cross else lens_arg, DT,
+                                        P(err), sp)
         ev[-1].record(stream)
         if rc != 0:
             raise RuntimeError("launch failed with status %d" % rc)
@@ -494,6 +497,27 @@ def kernel_rows(res, pk):
     return rows
 
 
+KERNEL_FILES = {"attention": "attn_tc.cu", "qkv_projection": "gemm_tc.cu",
+                "output_projection": "gemm_tc.cu"}
+
+
+def roofline(w, krows, pk, pk_kind, dev):
+    """Roofline of the workload's dominant kernel (the largest time): the
+    achieved TFLOP/s (effective count) over the measured bf16 peak, or, on
+    the fp32 path (CUDA cores), over the derived fp32 FMA peak; DRAM bytes per
+    launch from a committed ncu capture of the same kernel source."""
+    dom = max(krows, key=lambda k: krows[k]["ms"])
+    ach = krows[dom]["tflops"]
+    roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "peak_kind": pk_kind + " burst",
+            "ms_per_launch": krows[dom]["ms"], "traffic": stored_traffic(dom, w.name)}
+    if w.dtype == "f32":  # every kernel of the fp32 path runs on the CUDA cores
+        alu = alu_peak_tflops(dev, sm_max_mhz())
+        roof.update(bound="alu", peak=alu, frac=ach / alu,
+                    peak_kind="derived: SMs x 128 FP32 lanes x 2 flop x max SM clock")
+    return roof
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_setup(args.gpus)
@@ -509,17 +533,7 @@ def run_ours(args):
     fl = res["flops"]["total"]
     value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
     krows = kernel_rows(res, pk)
-    dom = max(krows, key=lambda k: krows[k]["ms"])
-    kernel_file = {"attention": "attn_tc.cu", "qkv_projection": "gemm_tc.cu",
-                   "output_projection": "gemm_tc.cu"}[dom]
-    ach = krows[dom]["tflops"]
-    roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "peak_kind": pk_kind + " burst",
-            "traffic": stored_traffic(dom, w.name)}
-    if w.dtype == "f32":  # every kernel of the fp32 path runs on the CUDA cores
-        alu = alu_peak_tflops(dev, sm_max_mhz())
-        roof.update(bound="alu", peak=alu, frac=ach / alu,
-                    peak_kind="derived: SMs x 128 FP32 lanes x 2 flop x max SM clock")
+    roof = roofline(w, krows, pk, pk_kind, dev)
     others = {}
     if not args.no_others and rank == 0:
         for j, wj in enumerate(workloads.WORKLOADS):
@@ -531,7 +545,7 @@ def run_ours(args):
             others[wj.name] = {"tflops": r["flops"]["total"] * len(r["per"]["step"])
                                / (r["total_ms"] * 1e-3) / 1e12,
                                "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
-                               "kernels": kr}
+                               "kernels": kr, "roofline": roofline(wj, kr, pk, pk_kind, dev)}
             del r
         # a general head size (d_h = 96): bf16 heads of 64..128 run in the
         # 128-wide tensor-core kernels, others on the CUDA cores (against the

@@ -5,7 +5,13 @@
 //   out: Y = Z W_O ("The Complete Multi-Head Operation").
 //
 // Persistent kernel, one CTA per SM, 128 x BN output tiles (BN = 256 or 128),
-// 64-deep K blocks in a STAGES-deep shared-memory ring filled by TMA:
+// 64-deep K blocks in a STAGES-deep shared-memory ring filled by TMA. The
+// problems that share their A operand (the QKV projections of one input) form
+// a group whose tiles run M panel by M panel, each 128-row panel of A through
+// every problem of the group back to back, so each panel is read from memory
+// once and then from L2. Panels that hold only padding rows are not
+// multiplied (skipped, or for the output projection written as zeros).
+//
 //   warp 0      TMA producer (one thread)
 //   warp 1      MMA issuer (one thread), owns the TMEM allocation
 //   warps 2..5  epilogue: TMEM -> registers -> bf16 -> global
@@ -23,17 +29,38 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 constexpr int MAXP = 3;
+constexpr int MAXRUNS = MHA_MAX_PADDED_BATCH + 1;
 
-struct GemmTcParams {
+// Launch parameters of the kernel; the run tables are sized by the template
+// argument so that launches with few runs (no selection, or a few batch
+// items) pass a small parameter block.
+struct GemmTcHead {
   CUtensorMap amap[MAXP];  // A: dims {K, M}, box {64, 128}, 128B swizzle
   CUtensorMap bmap[MAXP];  // W: dims {N, K}, box {64, 64}, 128B swizzle
   GemmProblem prob[MAXP];
-  int tiles_n[MAXP];       // N tiles per problem
-  int tile_start[MAXP + 1];
-  int nprob;
+  int tiles_n[MAXP];       // N tiles of each problem
+  int ngroups;
+  int g_first[MAXP + 1];   // problems [g_first[g], g_first[g + 1]) form group g
+  int g_ntiles[MAXP];      // N tiles of one M panel through all of group g
+  int g_select[MAXP];      // group g multiplies only the selected panels
+  int g_start[MAXP + 1];   // first tile of group g; g_start[ngroups]: product tiles
+  int zero_prob;           // problem whose unselected panels are written as zeros
+  int zero_tiles;          // tiles [g_start[ngroups], + zero_tiles): zero fills
+  int nrun, nzrun;
   int32_t* err;
   uint64_t limit_ns;
 };
+
+template <int RUNS>
+struct GemmTcParams {
+  GemmTcHead h;
+  int run_m[RUNS];    // selected panels: run r starts at panel run_m[r]
+  int run_pre[RUNS];  //   and is preceded by run_pre[r] selected panels
+  int zrun_m[RUNS];   // unselected panels, the same way
+  int zrun_pre[RUNS];
+};
+
+constexpr int SMALL_RUNS = 8;
 
 template <int BN>
 struct Cfg {
@@ -45,14 +72,49 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // double-buffered accumulator
 };
 
-__device__ __forceinline__ void decode_tile(const GemmTcParams& P, int t, int& p, int& m0,
-                                            int& n0, int bn) {
-  p = 0;
-  while (p + 1 < P.nprob && t >= P.tile_start[p + 1]) ++p;
-  const int local = t - P.tile_start[p];
-  const int tn = P.tiles_n[p];
-  m0 = (local / tn) * BM;
-  n0 = (local % tn) * bn;
+// The k-th panel of a run table (runs sorted, k below the table's total).
+__device__ __forceinline__ int panel_of(const int* run_m, const int* run_pre, int nrun, int k) {
+  int lo = 0, hi = nrun - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (run_pre[mid] <= k)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return run_m[lo] + (k - run_pre[lo]);
+}
+
+struct Tile {
+  int p, m0, n0;
+  bool zero;  // write zeros, no product
+};
+
+template <class Params>
+__device__ __forceinline__ Tile decode_tile(const Params& P, int t, int bn) {
+  const GemmTcHead& H = P.h;
+  Tile r;
+  const int prod = H.g_start[H.ngroups];
+  if (t >= prod) {
+    const int z = t - prod, tn = H.tiles_n[H.zero_prob];
+    r.p = H.zero_prob;
+    r.m0 = panel_of(P.zrun_m, P.zrun_pre, H.nzrun, z / tn) * BM;
+    r.n0 = (z % tn) * bn;
+    r.zero = true;
+    return r;
+  }
+  int g = 0;
+  while (g + 1 < H.ngroups && t >= H.g_start[g + 1]) ++g;
+  const int local = t - H.g_start[g];
+  const int k = local / H.g_ntiles[g];
+  int rr = local % H.g_ntiles[g];
+  int p = H.g_first[g];
+  while (rr >= H.tiles_n[p]) rr -= H.tiles_n[p++];
+  r.p = p;
+  r.m0 = (H.g_select[g] ? panel_of(P.run_m, P.run_pre, H.nrun, k) : k) * BM;
+  r.n0 = rr * bn;
+  r.zero = false;
+  return r;
 }
 
 // A bounded wait that ignores the abort flag: used only while draining
@@ -65,9 +127,35 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int BN>
-__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ GemmTcParams P) {
+// Stores one thread's 32 output columns [n, n + 32) of row m (packed bf16
+// pairs) through the problem's index map.
+__device__ __forceinline__ void store_row32(const GemmProblem& pr, long long row_off, int n,
+                                            const uint32_t (&pk)[16]) {
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(pr.out);
+  const long long off =
+      row_off + (long long)(n / pr.cols_per_group) * pr.s_group_col + (n % pr.cols_per_group);
+  if (n + 32 <= pr.N && (n % pr.cols_per_group) + 32 <= pr.cols_per_group) {
+    uint4* dst = reinterpret_cast<uint4*>(out + off);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  } else {
+    for (int j = 0; j < 32 && n + j < pr.N; ++j) {
+      const int nn = n + j;
+      const long long o = row_off + (long long)(nn / pr.cols_per_group) * pr.s_group_col +
+                          (nn % pr.cols_per_group);
+      const uint32_t word = pk[j >> 1];
+      const uint16_t bits = (j & 1) ? (uint16_t)(word >> 16) : (uint16_t)(word & 0xFFFF);
+      out[o] = __ushort_as_bfloat16(bits);
+    }
+  }
+}
+
+template <int BN, int RUNS>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ GemmTcParams<RUNS> P) {
   using C = Cfg<BN>;
+  const GemmTcHead& H = P.h;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -104,21 +192,22 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   // its outputs only once the previous kernel has completed.
   grid_dep_launch_dependents();
   grid_dep_wait();
-  const WaitCtl w{P.err, abort_flag, P.limit_ns};
-  const int total = P.tile_start[P.nprob];
+  const WaitCtl w{H.err, abort_flag, H.limit_ns};
+  const int prod = H.g_start[H.ngroups];       // tiles with a product
+  const int total = prod + H.zero_tiles;       // and the zero fills after them
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int p = 0; p < P.nprob; ++p) {
-        tma_prefetch_desc(&P.amap[p]);
-        tma_prefetch_desc(&P.bmap[p]);
+      for (int p = 0; p < MAXP; ++p) {
+        if (p >= H.g_first[H.ngroups]) break;
+        tma_prefetch_desc(&H.amap[p]);
+        tma_prefetch_desc(&H.bmap[p]);
       }
       uint32_t it = 0;  // global k-block counter across tiles
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int p, m0, n0;
-        decode_tile(P, t, p, m0, n0, BN);
-        const int kblocks = (P.prob[p].K + BK - 1) / BK;
+      for (int t = blockIdx.x; t < prod && ok; t += gridDim.x) {
+        const Tile tl = decode_tile(P, t, BN);
+        const int kblocks = (H.prob[tl.p].K + BK - 1) / BK;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % C::STAGES;
           if (it >= (uint32_t)C::STAGES && !mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, w)) {
@@ -128,10 +217,10 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
           uint8_t* a_s = smem + s * C::STAGE_BYTES;
           uint8_t* b_s = a_s + C::A_BYTES;
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          tma_load_2d(a_s, &P.amap[p], &full[s], kb * BK, m0);
+          tma_load_2d(a_s, &H.amap[tl.p], &full[s], kb * BK, tl.m0);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(b_s + j * (BK * 128), &P.bmap[p], &full[s], n0 + 64 * j, kb * BK);
+            tma_load_2d(b_s + j * (BK * 128), &H.bmap[tl.p], &full[s], tl.n0 + 64 * j, kb * BK);
         }
       }
       if (!ok) {  // let the loads this CTA started land before it exits
@@ -144,10 +233,9 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 1);
       uint32_t it = 0, tile_i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_i) {
-        int p, m0, n0;
-        decode_tile(P, t, p, m0, n0, BN);
-        const int kblocks = (P.prob[p].K + BK - 1) / BK;
+      for (int t = blockIdx.x; t < prod && ok; t += gridDim.x, ++tile_i) {
+        const Tile tl = decode_tile(P, t, BN);
+        const int kblocks = (H.prob[tl.p].K + BK - 1) / BK;
         const uint32_t buf = tile_i & 1;
         // wait until the epilogue has drained this accumulator buffer
         if (tile_i >= 2 && !mbar_wait(&acc_empty[buf], ((tile_i >> 1) - 1) & 1, w)) {
@@ -188,49 +276,45 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     // Epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4) .. +31.
     const int g = warp & 3;
     uint32_t tile_i = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_i) {
-      int p, m0, n0;
-      decode_tile(P, t, p, m0, n0, BN);
-      const uint32_t buf = tile_i & 1;
-      if (!mbar_wait(&acc_full[buf], (tile_i >> 1) & 1, w)) break;
-      tc_fence_after();
-      const GemmProblem& pr = P.prob[p];
-      const int m = m0 + 32 * g + lane;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile(P, t, BN);
+      const GemmProblem& pr = H.prob[tl.p];
+      const int m = tl.m0 + 32 * g + lane;
       const bool row_ok = m < pr.M;
       long long row_off = 0;
       if (row_ok)
         row_off = (long long)(m / pr.rows_per_group) * pr.s_group_row +
                   (long long)(m % pr.rows_per_group) * pr.s_row;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(pr.out);
+      if (tl.zero) {  // rows with nothing to multiply: zeros
+        if (!row_ok) continue;
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+        for (int c = 0; c < BN && tl.n0 + c < pr.N; c += 32) store_row32(pr, row_off, tl.n0 + c, pk);
+        continue;
+      }
+      const uint32_t buf = tile_i & 1;
+      const uint32_t phase = (tile_i >> 1) & 1;
+      ++tile_i;
+      if (!ok || !mbar_wait(&acc_full[buf], phase, w)) {
+        ok = false;
+        continue;  // the zero fills after the product tiles still run
+      }
+      tc_fence_after();
       const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(32 * g) << 16);
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
         tmem_ld32(taddr + c, r);
         tmem_wait_ld();
-        const int n = n0 + c;
+        const int n = tl.n0 + c;
         if (!row_ok || n >= pr.N) continue;
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-        const long long off = row_off + (long long)(n / pr.cols_per_group) * pr.s_group_col +
-                              (n % pr.cols_per_group);
-        if (n + 32 <= pr.N && (n % pr.cols_per_group) + 32 <= pr.cols_per_group) {
-          uint4* dst = reinterpret_cast<uint4*>(out + off);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        } else {
-          for (int j = 0; j < 32 && n + j < pr.N; ++j) {
-            const int nn = n + j;
-            const long long o = row_off + (long long)(nn / pr.cols_per_group) * pr.s_group_col +
-                                (nn % pr.cols_per_group);
-            const uint32_t word = pk[j >> 1];
-            const uint16_t bits = (j & 1) ? (uint16_t)(word >> 16) : (uint16_t)(word & 0xFFFF);
-            out[o] = __ushort_as_bfloat16(bits);
-          }
-        }
+        store_row32(pr, row_off, n, pk);
       }
       tc_fence_before();
       __syncwarp();
@@ -248,43 +332,120 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   }
 }
 
-template <int BN>
-mha_status launch(GemmTcParams& P, cudaStream_t s) {
+template <int BN, int RUNS>
+mha_status launch_kernel(const GemmTcParams<RUNS>& P, int grid, cudaStream_t s) {
   using C = Cfg<BN>;
-  int total = 0;
-  P.tile_start[0] = 0;
-  for (int i = 0; i < P.nprob; ++i) {
-    P.tiles_n[i] = (P.prob[i].N + BN - 1) / BN;
-    total += ((P.prob[i].M + BM - 1) / BM) * P.tiles_n[i];
-    P.tile_start[i + 1] = total;
-  }
-  for (int i = P.nprob; i < MAXP; ++i) P.tile_start[i + 1] = total;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return MHA_ERR_CUDA;
-    attr_set = true;
-  }
-  const int grid = total < num_sms() ? total : num_sms();
-  const cudaError_t e = launch_dependent(gemm_tc_kernel<BN>, dim3(grid), dim3(192), C::SMEM, s, P);
+  if (!ensure_smem_limit((const void*)gemm_tc_kernel<BN, RUNS>, C::SMEM)) return MHA_ERR_CUDA;
+  const cudaError_t e =
+      launch_dependent(gemm_tc_kernel<BN, RUNS>, dim3(grid), dim3(192), C::SMEM, s, P);
   count_launch();
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
+template <int BN>
+mha_status launch(GemmTcParams<MAXRUNS>& P, int nprob, int sel_panels, int unsel_panels,
+                  cudaStream_t s) {
+  GemmTcHead& H = P.h;
+  for (int i = 0; i < nprob; ++i) H.tiles_n[i] = (H.prob[i].N + BN - 1) / BN;
+  int start = 0;
+  for (int g = 0; g < H.ngroups; ++g) {
+    int nt = 0;
+    for (int p = H.g_first[g]; p < H.g_first[g + 1]; ++p) nt += H.tiles_n[p];
+    H.g_ntiles[g] = nt;
+    const GemmProblem& pr = H.prob[H.g_first[g]];
+    const long long panels = H.g_select[g] ? sel_panels : (pr.M + BM - 1) / BM;
+    H.g_start[g] = start;
+    const long long tiles = (long long)start + panels * nt;
+    if (tiles > (1ll << 30)) return MHA_ERR_UNSUPPORTED;
+    start = (int)tiles;
+  }
+  H.g_start[H.ngroups] = start;
+  H.zero_tiles = H.zero_prob >= 0 ? unsel_panels * H.tiles_n[H.zero_prob] : 0;
+  const int total = start + H.zero_tiles;
+  const int grid = total < num_sms() ? total : num_sms();
+  if (H.nrun <= SMALL_RUNS && H.nzrun <= SMALL_RUNS) {
+    GemmTcParams<SMALL_RUNS> Q;
+    Q.h = H;
+    for (int r = 0; r < SMALL_RUNS; ++r) {
+      Q.run_m[r] = P.run_m[r];
+      Q.run_pre[r] = P.run_pre[r];
+      Q.zrun_m[r] = P.zrun_m[r];
+      Q.zrun_pre[r] = P.zrun_pre[r];
+    }
+    return launch_kernel<BN, SMALL_RUNS>(Q, grid, s);
+  }
+  return launch_kernel<BN, MAXRUNS>(P, grid, s);
+}
+
+// Runs of selected and of unselected 128-row panels of the B * rows_per_batch
+// rows: panel k is selected when it holds a row j < need[b] of some batch item
+// b. Returns false when a table would overflow.
+bool build_runs(const RowSelect& sel, GemmTcParams<MAXRUNS>& P, int& sel_panels,
+                int& unsel_panels) {
+  const long long T = sel.rows_per_batch;
+  const long long panels = (sel.B * T + BM - 1) / BM;
+  int n = 0, cnt = 0;
+  long long last_end = -1;  // one past the last selected panel so far
+  for (int b = 0; b < sel.B; ++b) {
+    const long long first = b * T / BM, end = (b * T + sel.need[b] - 1) / BM + 1;
+    if (n > 0 && first <= last_end) {  // overlaps or touches the current run
+      if (end > last_end) {
+        cnt += (int)(end - last_end);
+        last_end = end;
+      }
+      continue;
+    }
+    if (n >= MAXRUNS) return false;
+    P.run_m[n] = (int)first;
+    P.run_pre[n] = cnt;
+    ++n;
+    cnt += (int)(end - first);
+    last_end = end;
+  }
+  P.h.nrun = n;
+  sel_panels = cnt;
+  // the complement
+  int z = 0, zc = 0;
+  long long pos = 0;
+  for (int r = 0; r <= n; ++r) {
+    const long long gap_end = r < n ? P.run_m[r] : panels;
+    const long long run_len = r < n ? (r + 1 < n ? P.run_pre[r + 1] : cnt) - P.run_pre[r] : 0;
+    if (gap_end > pos) {
+      if (z >= MAXRUNS) return false;
+      P.zrun_m[z] = (int)pos;
+      P.zrun_pre[z] = zc;
+      ++z;
+      zc += (int)(gap_end - pos);
+    }
+    pos = gap_end + run_len;
+  }
+  P.h.nzrun = z;
+  unsel_panels = zc;
+  return true;
+}
+
 }  // namespace
 
-mha_status gemm_tc(const GemmProblem* probs, int nprob, int32_t* err, cudaStream_t s) {
+mha_status gemm_tc(const GemmProblem* probs, int nprob, const RowSelect* sel, int32_t* err,
+                   cudaStream_t s) {
   if (nprob < 1 || nprob > MAXP) return MHA_ERR_INVALID_ARG;
-  GemmTcParams P;
+  static thread_local GemmTcParams<MAXRUNS> P;  // 17 KB: off the stack
   memset(&P, 0, sizeof(P));
-  P.nprob = nprob;
-  P.err = err;
-  P.limit_ns = wait_limit_ns();
+  GemmTcHead& H = P.h;
+  H.err = err;
+  H.limit_ns = wait_limit_ns();
+  H.zero_prob = -1;
   bool all256 = true;
+  int nsel = 0;
   for (int i = 0; i < nprob; ++i) {
     const GemmProblem& pr = probs[i];
-    P.prob[i] = pr;
+    H.prob[i] = pr;
+    if (pr.select) {
+      if (!sel || sel->B < 1 || sel->B > MHA_MAX_PADDED_BATCH ||
+          (long long)sel->B * sel->rows_per_batch != pr.M)
+        return MHA_ERR_INVALID_ARG;
+      ++nsel;
+    }
     if (pr.N % 256) all256 = false;
     // A: row-major M x K (K contiguous).
     const uint64_t adims[2] = {(uint64_t)pr.K, (uint64_t)pr.M};
@@ -294,8 +455,8 @@ mha_status gemm_tc(const GemmProblem* probs, int nprob, int32_t* err, cudaStream
     const uint64_t bdims[2] = {(uint64_t)pr.N, (uint64_t)pr.K};
     const uint64_t bstr[1] = {(uint64_t)pr.N * 2};
     const uint32_t bbox[2] = {64, BK};
-    if (!make_tmap_bf16(&P.amap[i], pr.A, 2, adims, astr, abox, true) ||
-        !make_tmap_bf16(&P.bmap[i], pr.W, 2, bdims, bstr, bbox, true))
+    if (!make_tmap_bf16(&H.amap[i], pr.A, 2, adims, astr, abox, true) ||
+        !make_tmap_bf16(&H.bmap[i], pr.W, 2, bdims, bstr, bbox, true))
       return MHA_ERR_CUDA;
     // 16-byte vector stores in the epilogue: every row pitch, group stride and
     // 32-column chunk offset is a multiple of 8 elements
@@ -303,7 +464,31 @@ mha_status gemm_tc(const GemmProblem* probs, int nprob, int32_t* err, cudaStream
         pr.s_group_row % 8)
       return MHA_ERR_UNSUPPORTED;
   }
-  return all256 ? launch<256>(P, s) : launch<128>(P, s);
+  // groups: neighbours with the same A operand and the same row selection
+  H.ngroups = 0;
+  for (int i = 0; i < nprob; ++i) {
+    const GemmProblem& pr = probs[i];
+    const bool join = i > 0 && pr.A == probs[i - 1].A && pr.M == probs[i - 1].M &&
+                      pr.K == probs[i - 1].K && pr.select == probs[i - 1].select;
+    if (!join) {
+      H.g_first[H.ngroups] = i;
+      H.g_select[H.ngroups] = pr.select;
+      ++H.ngroups;
+    }
+  }
+  H.g_first[H.ngroups] = nprob;
+  int sel_panels = 0, unsel_panels = 0;
+  if (nsel > 0) {
+    for (int b = 0; b < sel->B; ++b)
+      if (sel->need[b] < 1 || sel->need[b] > sel->rows_per_batch) return MHA_ERR_INVALID_ARG;
+    if (!build_runs(*sel, P, sel_panels, unsel_panels)) return MHA_ERR_UNSUPPORTED;
+    if (sel->zero_rest) {
+      if (nprob != 1) return MHA_ERR_INVALID_ARG;
+      H.zero_prob = 0;
+    }
+  }
+  return all256 ? launch<256>(P, nprob, sel_panels, unsel_panels, s)
+                : launch<128>(P, nprob, sel_panels, unsel_panels, s);
 }
 
 }  // namespace mha

@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -28,6 +29,54 @@ int num_sms() {
       cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     return 148;
   return n;
+}
+
+// Per-device kernel set-up, cached under one lock.
+namespace {
+struct KernelSetup {
+  const void* kernel;
+  int dev;
+  int smem_limit;  // dynamic shared memory raised to this (0: not set)
+  int resident;    // CTAs per SM (0: not asked)
+};
+std::mutex g_setup_mu;
+std::vector<KernelSetup> g_setup;
+
+KernelSetup* find_setup(const void* kernel, int dev) {
+  for (auto& k : g_setup)
+    if (k.kernel == kernel && k.dev == dev) return &k;
+  g_setup.push_back({kernel, dev, 0, 0});
+  return &g_setup.back();
+}
+}  // namespace
+
+bool ensure_smem_limit(const void* kernel, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  KernelSetup* k = find_setup(kernel, dev);
+  if (k->smem_limit >= bytes) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  k->smem_limit = bytes;
+  return true;
+}
+
+int resident_ctas(const void* kernel, int threads, int smem_bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  KernelSetup* k = find_setup(kernel, dev);
+  if (k->resident < 1) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes) !=
+            cudaSuccess ||
+        n < 1)
+      n = 1;
+    k->resident = n;
+  }
+  return k->resident;
 }
 
 // ---------------------------------------------------------------------------
@@ -168,19 +217,38 @@ mha_status check_valid_len(mha_mask_kind mask, const int32_t* valid_len, int B, 
   return MHA_OK;
 }
 
+// Key blocks of the attention kernels are 128 keys: with a padding mask the
+// rows of K and V up to the valid length rounded up to a block are read (those
+// past the length with weight exactly 0, so they must be finite), rows beyond
+// are never read.
+constexpr int KEY_BLOCK = 128;
+
 // The three projections as one grouped GEMM: X_q (d_q wide) W_Q, X_k (d_k
-// wide) W_K, X_v (d_v wide) W_V, each written head-split.
+// wide) W_K, X_v (d_v wide) W_V, each written head-split. With valid lengths
+// (a padding mask) only the rows the attention step reads are computed: K and
+// V rows below L_b rounded up to a key block, and the same Q rows when the
+// query rows are positions of the same sequence (self_attention).
 mha_status run_qkv(const void* X_q, const void* X_k, const void* X_v, const void* W_Q,
                    const void* W_K, const void* W_V, void* Q, void* K, void* V, int B, int n_q,
-                   int n_k, int d_q, int d_k, int d_v, int h, int d_h, int d_vh, mha_dtype dt,
-                   int32_t* err, cudaStream_t s) {
+                   int n_k, int d_q, int d_k, int d_v, int h, int d_h, int d_vh,
+                   const int32_t* valid_len, int self_attention, mha_dtype dt, int32_t* err,
+                   cudaStream_t s) {
   GemmProblem p[3] = {
       head_split_problem(X_q, W_Q, Q, B, n_q, h, d_h, d_q),
       head_split_problem(X_k, W_K, K, B, n_k, h, d_h, d_k),
       head_split_problem(X_v, W_V, V, B, n_k, h, d_vh, d_v),
   };
-  if (dt == MHA_DTYPE_BF16) return gemm_tc(p, 3, err, s);
-  return gemm_simt(p, 3, dt, s);
+  if (dt != MHA_DTYPE_BF16) return gemm_simt(p, 3, dt, s);
+  if (!valid_len) return gemm_tc(p, 3, nullptr, err, s);
+  int32_t need[MHA_MAX_PADDED_BATCH];
+  for (int b = 0; b < B; ++b) {
+    const long long r = ((long long)valid_len[b] + KEY_BLOCK - 1) / KEY_BLOCK * KEY_BLOCK;
+    need[b] = (int32_t)(r < n_k ? r : n_k);
+  }
+  RowSelect sel{B, n_k, need, 0};
+  p[0].select = self_attention ? 1 : 0;
+  p[1].select = p[2].select = 1;
+  return gemm_tc(p, 3, &sel, err, s);
 }
 
 // bf16 alignment the tensor-memory-access (TMA) GEMM needs: 16-byte row
@@ -194,11 +262,18 @@ mha_status run_attention(const AttnArgs& a, mha_dtype dt, cudaStream_t s) {
   return attention_simt(a, dt, s);
 }
 
+// Y = Z W_O. With valid lengths (padded query rows of self-attention), the
+// 128-row panels that hold only rows i >= L_b are written as zeros without a
+// product (their Z rows are zeros); other rows are multiplied as usual.
 mha_status run_out(const void* Z, const void* W_O, void* Y, int B, int n_q, int h, int d_vh,
-                   int d_o, mha_dtype dt, int32_t* err, cudaStream_t s) {
+                   int d_o, const int32_t* valid_len, mha_dtype dt, int32_t* err,
+                   cudaStream_t s) {
   GemmProblem p = plain_problem(Z, W_O, Y, B * n_q, d_o, h * d_vh);
-  if (dt == MHA_DTYPE_BF16) return gemm_tc(&p, 1, err, s);
-  return gemm_simt(&p, 1, dt, s);
+  if (dt != MHA_DTYPE_BF16) return gemm_simt(&p, 1, dt, s);
+  if (!valid_len) return gemm_tc(&p, 1, nullptr, err, s);
+  RowSelect sel{B, n_q, valid_len, 1};
+  p.select = 1;
+  return gemm_tc(&p, 1, &sel, err, s);
 }
 
 // The attention step with its checks; head_gate (host, h floats) may be null.
@@ -274,13 +349,16 @@ mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h, int d_v
 mha_status mha_qkv_projection(const void* X_q, const void* X_kv, const void* W_Q,
                               const void* W_K, const void* W_V, void* Q, void* K, void* V,
                               int B, int n_q, int n_k, int d_model, int h, int d_h, int d_vh,
-                              mha_dtype dt, int32_t* dev_error, void* stream) {
+                              mha_mask_kind mask, const int32_t* valid_len, mha_dtype dt,
+                              int32_t* dev_error, void* stream) {
   if (!X_q || !W_Q || !W_K || !W_V || !Q || !K || !V) return MHA_ERR_INVALID_ARG;
   if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
     return MHA_ERR_INVALID_ARG;
-  if (!dtype_ok(dt)) return MHA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt) || !mask_ok(mask)) return MHA_ERR_INVALID_ARG;
   if (!X_kv && n_k != n_q) return MHA_ERR_INVALID_ARG;
-  mha_status st = check_head_dims(d_h, d_vh, dt);
+  mha_status st = check_valid_len(mask, valid_len, B, n_k);
+  if (st != MHA_OK) return st;
+  st = check_head_dims(d_h, d_vh, dt);
   if (st != MHA_OK) return st;
   if (!fits(B, n_q, d_model) || !fits(B, n_k, d_model) || !fits(B, n_q, h * d_h) ||
       !fits(B, n_k, h * (long long)d_vh))
@@ -293,7 +371,8 @@ mha_status mha_qkv_projection(const void* X_q, const void* X_kv, const void* W_Q
       return MHA_ERR_UNSUPPORTED;
   }
   return run_qkv(X_q, Xk, Xk, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_model, d_model, d_model, h,
-                 d_h, d_vh, dt, dev_error, static_cast<cudaStream_t>(stream));
+                 d_h, d_vh, has_padding(mask) ? valid_len : nullptr, X_kv ? 0 : 1, dt, dev_error,
+                 static_cast<cudaStream_t>(stream));
 }
 
 mha_status mha_attention(const void* Q, const void* K, const void* V, void* Z, int B, int n_q,
@@ -305,16 +384,20 @@ mha_status mha_attention(const void* Q, const void* K, const void* V, void* Z, i
 }
 
 mha_status mha_output_projection(const void* Z, const void* W_O, void* Y, int B, int n_q, int h,
-                                 int d_vh, int d_o, mha_dtype dt, int32_t* dev_error,
-                                 void* stream) {
+                                 int d_vh, int d_o, const int32_t* valid_len, mha_dtype dt,
+                                 int32_t* dev_error, void* stream) {
   if (!Z || !W_O || !Y) return MHA_ERR_INVALID_ARG;
   if (B <= 0 || n_q <= 0 || h <= 0 || d_vh <= 0 || d_o <= 0) return MHA_ERR_INVALID_ARG;
   if (!dtype_ok(dt)) return MHA_ERR_INVALID_ARG;
+  if (valid_len) {
+    const mha_status st = check_valid_len(MHA_MASK_PADDING, valid_len, B, n_q);
+    if (st != MHA_OK) return st;
+  }
   if (!fits(B, n_q, (long long)h * d_vh) || !fits(B, n_q, d_o)) return MHA_ERR_UNSUPPORTED;
   if (dt == MHA_DTYPE_BF16 &&
       ((h * d_vh) % 8 || d_o % 8 || !aligned16(Z) || !aligned16(W_O) || !aligned16(Y)))
     return MHA_ERR_UNSUPPORTED;
-  return run_out(Z, W_O, Y, B, n_q, h, d_vh, d_o, dt, dev_error,
+  return run_out(Z, W_O, Y, B, n_q, h, d_vh, d_o, valid_len, dt, dev_error,
                  static_cast<cudaStream_t>(stream));
 }
 
@@ -363,13 +446,16 @@ mha_status mha_forward_general(const void* X_q, const void* X_k, const void* X_v
   void* V = ws + L.v;
   void* Z = ws + L.z;
   if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return MHA_ERR_CUDA;
+  const int32_t* lens = has_padding(mask) ? valid_len : nullptr;
   st = run_qkv(X_q, X_k, X_v, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_q, d_k, d_v, h, d_h, d_vh,
-               dt, err, s);
+               lens, self_attention ? 1 : 0, dt, err, s);
   if (st != MHA_OK) return st;
   st = attention_step(Q, K, V, Z, B, n_q, n_k, h, d_h, d_vh, c, mask, valid_len,
                       self_attention ? 1 : 0, head_gate, dt, err, stream);
   if (st != MHA_OK) return st;
-  return mha_output_projection(Z, W_O, Y, B, n_q, h, d_vh, d_o, dt, err, stream);
+  // padded query rows (self-attention) are zeros in Z, so in Y
+  return mha_output_projection(Z, W_O, Y, B, n_q, h, d_vh, d_o, self_attention ? lens : nullptr,
+                               dt, err, stream);
 }
 
 mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_Q, const void* W_K,

@@ -71,11 +71,11 @@ def load(path=LIB_PATH):
     lib.mha_forward_no_alloc.restype = I
     lib.mha_forward_no_alloc.argtypes = [P] * 7 + [I] * 8 + [F, I, P, I, P]
     lib.mha_qkv_projection.restype = I
-    lib.mha_qkv_projection.argtypes = [P] * 8 + [I] * 7 + [I, P, P]
+    lib.mha_qkv_projection.argtypes = [P] * 8 + [I] * 7 + [I, P, I, P, P]
     lib.mha_attention.restype = I
     lib.mha_attention.argtypes = [P] * 4 + [I] * 6 + [F, I, P, I, I, P, P]
     lib.mha_output_projection.restype = I
-    lib.mha_output_projection.argtypes = [P] * 3 + [I] * 5 + [I, P, P]
+    lib.mha_output_projection.argtypes = [P] * 3 + [I] * 5 + [P, I, P, P]
     lib.mha_get_device_error.restype = I
     lib.mha_get_device_error.argtypes = [P, P]
     lib.mha_status_string.restype = ctypes.c_char_p
@@ -250,19 +250,25 @@ def forward_no_alloc(X_q, X_kv, W_Q, W_K, W_V, W_O, h, d_h, d_vh, c, mask="none"
     return out
 
 
-def qkv_projection(X_q, X_kv, W_Q, W_K, W_V, h, d_h, d_vh, dev_error=None, stream=None):
-    """Step 1: head-split Q (B,h,n_q,d_h), K (B,h,n_k,d_h), V (B,h,n_k,d_vh)."""
+def qkv_projection(X_q, X_kv, W_Q, W_K, W_V, h, d_h, d_vh, mask="none", valid_len=None,
+                   out=None, dev_error=None, stream=None):
+    """Step 1: head-split Q (B,h,n_q,d_h), K (B,h,n_k,d_h), V (B,h,n_k,d_vh).
+    With a padding mask only the rows the attention step reads are written
+    (below valid_len[b] rounded up to 128). out: (Q, K, V) to write into."""
     lib = load()
     B, n_q, d_model = X_q.shape
     n_k = n_q if X_kv is None else X_kv.shape[1]
     dt = TORCH_DTYPES[X_q.dtype]
     kw = dict(dtype=X_q.dtype, device=X_q.device)
-    Q = torch.empty((B, h, n_q, d_h), **kw)
-    K = torch.empty((B, h, n_k, d_h), **kw)
-    V = torch.empty((B, h, n_k, d_vh), **kw)
+    if out is None:
+        out = (torch.empty((B, h, n_q, d_h), **kw), torch.empty((B, h, n_k, d_h), **kw),
+               torch.empty((B, h, n_k, d_vh), **kw))
+    Q, K, V = out
+    lens, keep = _lens(valid_len, B)
     st = lib.mha_qkv_projection(_ptr(X_q), _ptr(X_kv), _ptr(W_Q), _ptr(W_K), _ptr(W_V),
                                 _ptr(Q), _ptr(K), _ptr(V), B, n_q, n_k, d_model, h, d_h, d_vh,
-                                DTYPES[dt], _ptr(dev_error), _stream(stream))
+                                MASKS[mask], lens, DTYPES[dt], _ptr(dev_error), _stream(stream))
+    del keep
     _check(st, "mha_qkv_projection")
     return Q, K, V
 
@@ -285,16 +291,19 @@ def attention(Q, K, V, c, mask="none", valid_len=None, self_attention=True, out=
     return out
 
 
-def output_projection(Z, W_O, h, d_vh, out=None, dev_error=None, stream=None):
-    """Step 3: Y = Z W_O."""
+def output_projection(Z, W_O, h, d_vh, valid_len=None, out=None, dev_error=None, stream=None):
+    """Step 3: Y = Z W_O. valid_len (self-attention padding): the rows
+    i >= valid_len[b] are padded query rows, zero in Z and written as zeros."""
     lib = load()
     B, n_q, _ = Z.shape
     d_o = W_O.shape[1]
     dt = TORCH_DTYPES[Z.dtype]
     if out is None:
         out = torch.empty((B, n_q, d_o), dtype=Z.dtype, device=Z.device)
-    st = lib.mha_output_projection(_ptr(Z), _ptr(W_O), _ptr(out), B, n_q, h, d_vh, d_o,
+    lens, keep = _lens(valid_len, B)
+    st = lib.mha_output_projection(_ptr(Z), _ptr(W_O), _ptr(out), B, n_q, h, d_vh, d_o, lens,
                                    DTYPES[dt], _ptr(dev_error), _stream(stream))
+    del keep
     _check(st, "mha_output_projection")
     return out
 

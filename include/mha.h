@@ -204,11 +204,20 @@ MHA_API mha_status mha_forward_general(const void* X_q, const void* X_k, const v
  *   V (B, h, n_k, d_vh) = head split of X_kv W_V
  * X_kv NULL means X_kv := X_q (n_k must equal n_q). dev_error: device int32
  * error word (may be NULL: timeouts then go unreported).
+ * mask, valid_len: as for mha_attention. With a padding mask (bf16) only the
+ * rows mha_attention reads are computed: rows j < valid_len[b] rounded up to
+ * a multiple of 128 (capped at n_k) of K and V, and the same rows of Q for
+ * self-attention (X_kv NULL); the rows past them are left as they were. The
+ * rows between valid_len[b] and that bound are computed because mha_attention
+ * reads them (with weight exactly 0, so they must be finite).
+ * MHA_ERR_INVALID_ARG for a padding mask without valid_len, MHA_ERR_EMPTY_ROW
+ * for a length outside [1, n_k].
  */
 MHA_API mha_status mha_qkv_projection(const void* X_q, const void* X_kv,
                               const void* W_Q, const void* W_K, const void* W_V,
                               void* Q, void* K, void* V, int B, int n_q,
                               int n_k, int d_model, int h, int d_h, int d_vh,
+                              mha_mask_kind mask, const int32_t* valid_len,
                               mha_dtype dt, int32_t* dev_error, void* stream);
 
 /*
@@ -253,11 +262,16 @@ MHA_API mha_status mha_attention_plan(int B, int n_q, int n_k, int h, int d_h, i
 /*
  * Step 3: Y (B*n_q, d_o) = Z (B*n_q, h*d_vh) W_O (h*d_vh, d_o)
  * ("The Complete Multi-Head Operation": Y = Z W_O).
+ * valid_len: HOST int32[B] or NULL. Given, the rows i >= valid_len[b] of
+ * batch item b are the padded query rows of self-attention, whose Z rows
+ * mha_attention writes as zeros: Y there is zero, and (bf16) 128-row panels
+ * made only of such rows are written as zeros without a product.
+ * MHA_ERR_EMPTY_ROW for a length outside [1, n_q].
  */
 MHA_API mha_status mha_output_projection(const void* Z, const void* W_O, void* Y,
                                  int B, int n_q, int h, int d_vh, int d_o,
-                                 mha_dtype dt, int32_t* dev_error,
-                                 void* stream);
+                                 const int32_t* valid_len, mha_dtype dt,
+                                 int32_t* dev_error, void* stream);
 
 /*
  * Device scratch for mha_attention_decode, in bytes: one partial summary

@@ -116,10 +116,20 @@ def test_steps_reject_bad_arguments_on_host(lib):
                              None, 1, 1, None, None) == 1
     assert lib.mha_attention(P(16), P(32), P(48), P(64), 1, 8, 8, 1, 64, 64, 0.1, 2, None, 1,
                              1, None, None) == 1
-    assert lib.mha_output_projection(None, P(16), P(32), 1, 8, 1, 64, 64, 1, None, None) == 1
-    assert lib.mha_output_projection(P(16), P(32), P(48), 1, 8, 1, 64, 12, 1, None, None) == 2
+    assert lib.mha_output_projection(None, P(16), P(32), 1, 8, 1, 64, 64, None, 1, None,
+                                     None) == 1
+    assert lib.mha_output_projection(P(16), P(32), P(48), 1, 8, 1, 64, 12, None, 1, None,
+                                     None) == 2
     assert lib.mha_qkv_projection(P(16), None, P(32), P(48), P(64), P(80), P(96), P(112), 1, 8,
-                                  9, 64, 1, 64, 64, 1, None, None) == 1
+                                  9, 64, 1, 64, 64, 0, None, 1, None, None) == 1
+    # padding without lengths; a length outside [1, n_k] / [1, n_q]
+    assert lib.mha_qkv_projection(P(16), None, P(32), P(48), P(64), P(80), P(96), P(112), 1, 8,
+                                  8, 64, 1, 64, 64, 2, None, 1, None, None) == 1
+    lens, keep = _lens(9)
+    assert lib.mha_qkv_projection(P(16), None, P(32), P(48), P(64), P(80), P(96), P(112), 1, 8,
+                                  8, 64, 1, 64, 64, 2, lens, 1, None, None) == 3
+    assert lib.mha_output_projection(P(16), P(32), P(48), 1, 8, 1, 64, 64, lens, 1, None,
+                                     None) == 3
     assert lib.mha_get_device_error(None, None) == 1
     assert lib.mha_selftest_wait_timeout(None, 1000, None) == 1
 

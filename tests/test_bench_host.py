@@ -54,7 +54,8 @@ def test_reference_arm_prints_one_json_line():
     # the same workload keys as the GPU arm's line, the default workload
     import bench
     from head_scaled_dot_gb300 import workloads
-    w = workloads.WORKLOADS[1]
-    for k, v in bench.workload_config(w, None).items():
+    w = workloads.WORKLOADS[3]
+    lens = [int(x) for x in workloads.make_inputs(w)["valid_len"]]
+    for k, v in bench.workload_config(w, lens).items():
         assert d["config"][k] == v, k
     assert d["metric"] == bench.METRIC and d["higher_is_better"] is True

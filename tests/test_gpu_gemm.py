@@ -69,3 +69,84 @@ def test_qkv_projection_head_split(B, T, n_k, d_model, h, d_h, d_vh, cross):
                                   d_vh, 0.1, return_intermediates=True)
     for name, got in (("Q", Q), ("K", K), ("V", V)):
         assert rel_err(f64(got), inter[name]) <= 4e-3, name
+
+
+@pytest.mark.parametrize("B,T,n_k,lens,cross", [
+    (3, 300, 300, [300, 131, 1], False),   # panels span batch items (T % 128 != 0)
+    (2, 1024, 1024, [129, 1000], False),
+    (4, 64, 200, [1, 200, 129, 128], True),  # cross: keys only
+])
+def test_qkv_projection_computes_only_the_rows_attention_reads(B, T, n_k, lens, cross):
+    """With a padding mask the projection writes the rows below valid_len[b]
+    rounded up to 128 (K and V; Q too for self-attention) and leaves every
+    other row as it was (NaN here)."""
+    d_model, h, d_h, d_vh = 128, 2, 64, 128
+    g = torch.Generator().manual_seed(B * T + n_k)
+    X = bf16((B, T, d_model), g)
+    Xkv = bf16((B, n_k, d_model), g) if cross else None
+    WQ = bf16((d_model, h * d_h), g, d_model ** -0.5)
+    WK = bf16((d_model, h * d_h), g, d_model ** -0.5)
+    WV = bf16((d_model, h * d_vh), g, d_model ** -0.5)
+    nk = n_k if cross else T
+    nan = lambda *s: torch.full(s, float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = (nan(B, h, T, d_h), nan(B, h, nk, d_h), nan(B, h, nk, d_vh))
+    Q, K, V = mha.qkv_projection(X.cuda(), None if Xkv is None else Xkv.cuda(), WQ.cuda(),
+                                 WK.cuda(), WV.cuda(), h, d_h, d_vh, mask="padding",
+                                 valid_len=lens, out=out)
+    torch.cuda.synchronize()
+    _, inter = oracle.mha_forward(f64(X), f64(Xkv), f64(WQ), f64(WK), f64(WV),
+                                  f64(bf16((h * d_vh, 8), g)), h, d_h, d_vh, 0.1,
+                                  return_intermediates=True)
+    for name, got, rows_sel in (("Q", Q, not cross), ("K", K, True), ("V", V, True)):
+        got = f64(got)
+        n = got.shape[2]
+        for b in range(B):
+            need = min(n, (lens[b] + 127) // 128 * 128) if rows_sel else n
+            assert rel_err(got[b, :, :need], inter[name][b, :, :need]) <= 4e-3, name
+            # rows past `need` may be written only where a 128-row panel of
+            # the flattened B * n rows also holds needed rows of a neighbour
+            panel_lo = ((b * n + need) + 127) // 128 * 128 - b * n
+            nxt = (b + 1) * n  # the next batch item's rows start there
+            untouched_to = min(n, ((nxt // 128) * 128 - b * n) if b + 1 < B else n)
+            if panel_lo < untouched_to:
+                assert np.isnan(got[b, :, panel_lo:untouched_to]).all(), name
+
+
+@pytest.mark.parametrize("B,T,lens", [(3, 300, [300, 1, 131]), (2, 1024, [100, 1024]),
+                                      (5, 128, [1, 128, 64, 127, 2])])
+def test_output_projection_zero_rows_past_the_valid_length(B, T, lens):
+    """Rows i >= valid_len[b] of Y are exact zeros (their Z rows are zeros,
+    as the attention step writes them); panels made only of such rows are
+    written without a product, the rest are multiplied as usual."""
+    K, N = 192, 256
+    g = torch.Generator().manual_seed(B * T)
+    Z = bf16((B, T, K), g)
+    for b, L in enumerate(lens):
+        Z[b, L:] = 0
+    W = bf16((K, N), g, K ** -0.5)
+    Y = torch.full((B, T, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mha.output_projection(Z.cuda(), W.cuda(), 1, K, valid_len=lens, out=Y)
+    torch.cuda.synchronize()
+    got = f64(Y)
+    ref = f64(Z) @ f64(W)
+    assert np.isfinite(got).all()
+    for b, L in enumerate(lens):
+        assert np.all(got[b, L:] == 0.0)
+    assert rel_err(got, ref) <= 4e-3
+
+
+def test_general_form_three_inputs_three_groups():
+    """Separate X_q, X_k, X_v buffers (three A operands, three groups of the
+    grouped launch) against the oracle, padding on keys."""
+    B, n_q, n_k, d_q, d_k, d_v, h, d = 2, 140, 300, 64, 96, 128, 2, 64
+    g = torch.Generator().manual_seed(77)
+    X_q, X_k, X_v = bf16((B, n_q, d_q), g), bf16((B, n_k, d_k), g), bf16((B, n_k, d_v), g)
+    W_Q, W_K = bf16((d_q, h * d), g, d_q ** -0.5), bf16((d_k, h * d), g, d_k ** -0.5)
+    W_V, W_O = bf16((d_v, h * d), g, d_v ** -0.5), bf16((h * d, 72), g, (h * d) ** -0.5)
+    lens = [5, 300]
+    Y = mha.forward_general(X_q.cuda(), X_k.cuda(), X_v.cuda(), W_Q.cuda(), W_K.cuda(),
+                            W_V.cuda(), W_O.cuda(), h, d, d, 0.125, "padding", lens)
+    torch.cuda.synchronize()
+    ref = oracle.mha_forward_general(f64(X_q), f64(X_k), f64(X_v), f64(W_Q), f64(W_K), f64(W_V),
+                                     f64(W_O), h, d, d, 0.125, oracle.MASK_PADDING, lens, False)
+    assert rel_err(f64(Y), ref) <= 1e-2
