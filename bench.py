@@ -212,6 +212,11 @@ def measure_workload(w, steps, warmup, dev, world, e2e=True, sample_clocks=True)
     err, Qp, Kp, Vp, Zp = base, base + L["q"], base + L["k"], base + L["v"], base + L["z"]
     lens_arg, keep = mha._lens(lens, B)
     DT, MK = mha.DTYPES[w.dtype], mha.MASKS[w.mask]
+    # the scratch of the automatic split over the keys, after Z (as mha_forward
+    # lays it out); workloads with few query tiles run the attention step split
+    es = 2 if w.dtype == "bf16" else 4
+    split_off = L["z"] + (B * n_q * w.h * w.d_vh * es + 1023) // 1024 * 1024
+    split_bytes = L["total"] - split_off
     X_kv_p = None if t["X_kv"] is None else P(t["X_kv"].data_ptr())
 
     def step(ev):
@@ -227,8 +232,14 @@ def measure_workload(w, steps, warmup, dev, world, e2e=True, sample_clocks=True)
                                     lens_arg, DT, P(err), sp)
         if split:
             ev[1].record(stream)
-        rc |= lib.mha_attention(P(Qp), P(Kp), P(Vp), P(Zp), B, n_q, n_k, w.h, w.d_h, w.d_vh,
-                                float(w.c), MK, lens_arg, 0 if w.cross else 1, DT, P(err), sp)
+        if split_bytes > 0:
+            rc |= lib.mha_attention_split(P(Qp), P(Kp), P(Vp), P(Zp), B, n_q, n_k, w.h, w.d_h,
+                                          w.d_vh, float(w.c), MK, lens_arg, 0 if w.cross else 1,
+                                          0, DT, P(base + split_off), split_bytes, P(err), sp)
+        else:
+            rc |= lib.mha_attention(P(Qp), P(Kp), P(Vp), P(Zp), B, n_q, n_k, w.h, w.d_h,
+                                    w.d_vh, float(w.c), MK, lens_arg, 0 if w.cross else 1, DT,
+                                    P(err), sp)
         if split:
             ev[2].record(stream)
         rc |= lib.mha_output_projection(P(Zp), P(t["W_O"].data_ptr()), P(Y.data_ptr()), B, n_q,
@@ -571,6 +582,29 @@ def run_ours(args):
                            "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
                            "kernels": kr, "roofline": groof}
         del r
+        # few query rows against many keys: the attention step splits the keys
+        # over thread blocks and merges the summaries
+        for lw in workloads.LONG_KEYS:
+            r = measure_workload(lw, max(3, args.steps // 2), 3, dev, 1, e2e=False,
+                                 sample_clocks=False)
+            kr = kernel_rows(r, pk)
+            # 4 n_q d_h flop per key over 2 (d_h + d_vh) bytes of K and V: with
+            # n_q <= 128 below the ridge (peak flop / copy bandwidth), so the
+            # bound is reading Q, K, V and writing Z once
+            es = 2
+            nbytes = lw.B * lw.h * (lw.n_q * (lw.d_h + lw.d_vh) + lw.n_k * (lw.d_h + lw.d_vh)) * es
+            gbs = nbytes / (kr["attention"]["ms"] * 1e-3) / 1e9
+            lroof = {"kernel": "attention (keys split over thread blocks, summaries merged)",
+                     "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "bytes_per_launch": nbytes,
+                     "ms_per_launch": kr["attention"]["ms"],
+                     "attention_tflops": kr["attention"]["tflops"],
+                     "traffic": stored_traffic("attention", lw.name)}
+            others[lw.name] = {"tflops": r["flops"]["total"] * len(r["per"]["step"])
+                               / (r["total_ms"] * 1e-3) / 1e12,
+                               "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
+                               "kernels": kr, "roofline": lroof}
+            del r
         dw = workloads.DECODE
         others[dw.name] = measure_decode(dw, max(3, args.steps), 3, dev, pk)
     cpu = None

@@ -97,6 +97,13 @@ struct AttnTcParams {
   int causal, padding, pad_queries;
   int32_t* err;
   uint64_t limit_ns;
+  // Split over the keys (nsplit > 1): unit idx is split idx % nsplit of tile
+  // pair idx / nsplit and folds key blocks [split * split_blocks, ...) only;
+  // its summary goes to `part` and the last split of a tile to finish merges
+  // them (`split_cnt` counts the published splits of each tile).
+  int nsplit, split_blocks;
+  float* part;      // [pair][tile][split] slots of (DV + 2) x 128 floats
+  int* split_cnt;   // [pair][tile], zero on entry, left zero on exit
   int valid_len[MHA_MAX_PADDED_BATCH];
   int has_gate;                          // head_gate holds h entries (h <= MHA_MAX_GATED_HEADS)
   float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale, read only when has_gate
@@ -161,11 +168,15 @@ __device__ __forceinline__ int tile_blocks(const AttnTcParams& P, int tq0, int L
 }
 
 // One unit of work: the 128-row query tile starting at q0 of (b, head) and,
-// for a pair unit, the tile after it.
+// for a pair unit, the tile after it; with a split over the keys, only the
+// key blocks [kb0, kb0 + nmax) of them.
 struct Unit {
   int q0, head, b, L, q_end;
   int nb0, nb1, nmax;  // key blocks of tile 0, of tile 1, and the larger
   bool pair;           // tile 1 belongs to this unit (its rows are written here)
+  bool has0, has1;     // the tile has rows to compute (some key blocks in all)
+  int kb0;             // first key block of the unit
+  int split, pidx;     // split number and tile pair index (split summaries)
 };
 
 // Tile pairs are ordered pair-fastest within each (batch item, head), or,
@@ -173,12 +184,19 @@ struct Unit {
 // causal mask the heavy pairs (large q0) come first either way. Unit idx is
 // pair idx while idx < pair_units; after that, units pair_units + 2 j and
 // pair_units + 2 j + 1 are the two tiles of pair pair_units + j, on their own.
-__host__ __device__ inline void unit_coords(const AttnTcParams& P, int idx, int& pi, int& bh,
-                                            int& tile, bool& pair) {
-  int pidx = idx;
+// With a split over the keys every unit is a pair: unit idx is split
+// idx % nsplit of pair idx / nsplit.
+__host__ __device__ inline void unit_coords(const AttnTcParams& P, int nsplit, int idx, int& pi,
+                                            int& bh, int& tile, bool& pair, int& split,
+                                            int& pidx) {
+  pidx = idx;
   tile = 0;
+  split = 0;
   pair = true;
-  if (idx >= P.pair_units) {
+  if (nsplit > 1) {
+    pidx = idx / nsplit;
+    split = idx % nsplit;
+  } else if (idx >= P.pair_units) {
     const int j = idx - P.pair_units;
     pidx = P.pair_units + j / 2;
     tile = j & 1;
@@ -189,17 +207,37 @@ __host__ __device__ inline void unit_coords(const AttnTcParams& P, int idx, int&
   if (P.causal) pi = P.npair - 1 - pi;
 }
 
+// Blocks [kb0, kb0 + n) of a tile with nb blocks in all that fall in split s.
+__host__ __device__ inline int split_range(const AttnTcParams& P, int nsplit, int nb, int s,
+                                           int& kb0) {
+  if (nsplit <= 1) {
+    kb0 = 0;
+    return nb;
+  }
+  kb0 = s * P.split_blocks;
+  const int n = nb - kb0;
+  return n < 0 ? 0 : (n > P.split_blocks ? P.split_blocks : n);
+}
+
+// SPLIT: the kernel was launched for a split over the keys (P.nsplit > 1);
+// without it every unit folds all of its key blocks.
+template <bool SPLIT>
 __device__ __forceinline__ Unit unit_at(const AttnTcParams& P, int idx) {
   Unit u;
   int pi, bh, tile;
-  unit_coords(P, idx, pi, bh, tile, u.pair);
+  const int nsplit = SPLIT ? P.nsplit : 1;
+  unit_coords(P, nsplit, idx, pi, bh, tile, u.pair, u.split, u.pidx);
   u.head = bh % P.h;
   u.b = bh / P.h;
   u.q0 = pi * 2 * BLK_M + tile * BLK_M;
   u.L = P.padding ? P.valid_len[u.b] : P.n_k;
   u.q_end = P.pad_queries ? min(u.L, P.n_q) : P.n_q;
-  u.nb0 = tile_blocks(P, u.q0, u.L, u.q_end);
-  u.nb1 = (u.pair && u.q0 + BLK_M < P.n_q) ? tile_blocks(P, u.q0 + BLK_M, u.L, u.q_end) : 0;
+  const int f0 = tile_blocks(P, u.q0, u.L, u.q_end);
+  const int f1 = (u.pair && u.q0 + BLK_M < P.n_q) ? tile_blocks(P, u.q0 + BLK_M, u.L, u.q_end) : 0;
+  u.has0 = f0 > 0;
+  u.has1 = f1 > 0;
+  u.nb0 = split_range(P, nsplit, f0, u.split, u.kb0);
+  u.nb1 = split_range(P, nsplit, f1, u.split, u.kb0);
   u.nmax = u.nb1 > u.nb0 ? u.nb1 : u.nb0;  // tile 0's blocks are a prefix of tile 1's
   return u;
 }
@@ -235,7 +273,7 @@ struct Ring {
 // unit's first blocks load while the current unit's last ones are still
 // being used); each also asks L2 for the blocks PREFETCH ahead so that
 // refills come from L2.
-template <class C>
+template <class C, bool SPLIT>
 __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bool is_k,
                                         const WaitCtl& w) {
   const CUtensorMap* map = is_k ? &P.kmap : &P.vmap;
@@ -252,7 +290,7 @@ __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bo
   for (int i = 0; !gave_up; ++i) {
     const int idx = unit_index(P, i);
     if (idx < 0) break;
-    const Unit u = unit_at(P, idx);
+    const Unit u = unit_at<SPLIT>(P, idx);
     if (u.nmax == 0) continue;  // all rows padding: nothing to load
     const int bh = u.b * P.h + u.head;
     if (is_k) {
@@ -282,15 +320,17 @@ __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bo
       }
       mbar_arrive_expect_tx(&full[s], bytes);
       for (int p = 0; p < panels; ++p)
-        tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, kb * BLK_N, bh);
+        tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, (u.kb0 + kb) * BLK_N, bh);
       // L2 requests for the blocks past the ring, after the first block's
       // load so that they do not delay it
       if (kb == 0)
         for (int pk = C::STAGES; pk < C::STAGES + PREFETCH && pk < u.nmax; ++pk)
-          for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, pk * BLK_N, bh);
+          for (int p = 0; p < panels; ++p)
+            tma_prefetch_l2_3d(map, 64 * p, (u.kb0 + pk) * BLK_N, bh);
       const int ahead = kb + C::STAGES + PREFETCH;
       if (ahead < u.nmax)
-        for (int p = 0; p < panels; ++p) tma_prefetch_l2_3d(map, 64 * p, ahead * BLK_N, bh);
+        for (int p = 0; p < panels; ++p)
+          tma_prefetch_l2_3d(map, 64 * p, (u.kb0 + ahead) * BLK_N, bh);
     }
     ++ui;
   }
@@ -303,7 +343,95 @@ __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bo
   }
 }
 
-template <int DQK, int DV>
+// ---------------------------------------------------------------------------
+// Split over the keys: the summary of a split is published in a slot of its
+// own, (pair, tile, split): z column-major (column c of row r at c * 128 + r,
+// DV columns), then m[128] and l[128] (m in the scaled base-2 units of the
+// kernel, -inf for a split without a key block of the tile: the empty
+// summary). The thread block that publishes a tile's last split merges all
+// of the tile's summaries with the merge of the Definition (m' = max m_s,
+// l' = sum e^{m_s - m'} l_s, z' likewise) and writes z' / l' to Z. Nothing
+// waits on another thread block: the last one to arrive finds every other
+// summary already written.
+// ---------------------------------------------------------------------------
+
+template <int DV>
+__device__ __forceinline__ float* split_slot(const AttnTcParams& P, int pidx, int t, int s) {
+  return P.part + ((size_t)(pidx * 2 + t) * P.nsplit + s) * (size_t)((DV + 2) * BLK_M);
+}
+
+__device__ __forceinline__ void tile_sync(int bar_id) {
+  asm volatile("bar.sync %0, 256;" ::"r"(bar_id) : "memory");
+}
+
+// Called by all 256 softmax threads of tile t (named barrier bar_id) once the
+// thread's half row of z (columns [half DV/2, (half + 1) DV/2)) is in the
+// slot: publishes (m, l) of row r, counts the split, and in the last thread
+// block merges and stores row r's half of Z. flag: one shared int.
+template <int DV>
+__device__ void split_finish(const AttnTcParams& P, const Unit& u, int t, int r, int half,
+                             float m, float l, int bar_id, volatile int* flag) {
+  constexpr int HC = DV / 2;
+  float* slot = split_slot<DV>(P, u.pidx, t, u.split);
+  if (half == 0) {
+    __stcg(slot + DV * BLK_M + r, m);
+    __stcg(slot + (DV + 1) * BLK_M + r, l);
+  }
+  __threadfence();
+  tile_sync(bar_id);
+  if (r == 0 && half == 0) {
+    int* cnt = P.split_cnt + u.pidx * 2 + t;
+    const int last = atomicAdd(cnt, 1) == P.nsplit - 1;
+    if (last) atomicExch(cnt, 0);  // every split has counted: ready for the next call
+    __threadfence();
+    *flag = last;
+  }
+  tile_sync(bar_id);
+  if (!*flag) return;
+  __threadfence();
+  const int q = u.q0 + t * BLK_M + r;
+  if (q >= P.n_q) return;
+  const float* base = P.part + (size_t)(u.pidx * 2 + t) * P.nsplit * (size_t)((DV + 2) * BLK_M);
+  constexpr size_t SLOT = (size_t)(DV + 2) * BLK_M;
+  float M = -INFINITY;
+  for (int s = 0; s < P.nsplit; ++s) M = fmaxf(M, __ldcg(base + s * SLOT + DV * BLK_M + r));
+  float lsum = 0.f;
+  for (int s = 0; s < P.nsplit; ++s) {
+    const float ms = __ldcg(base + s * SLOT + DV * BLK_M + r);
+    if (ms != -INFINITY) lsum += exp2f(ms - M) * __ldcg(base + s * SLOT + (DV + 1) * BLK_M + r);
+  }
+  const bool computed = q < u.q_end;
+  const float inv = computed ? (P.has_gate ? P.head_gate[u.head] : 1.f) / lsum : 0.f;
+  __nv_bfloat16* zrow = static_cast<__nv_bfloat16*>(P.Z) +
+                        ((long long)u.b * P.n_q + q) * ((long long)P.h * P.dv) +
+                        (long long)u.head * P.dv + half * HC;
+#pragma unroll 1
+  for (int cb = 0; cb < HC / 32; ++cb) {
+    float acc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    if (computed) {
+      for (int s = 0; s < P.nsplit; ++s) {
+        const float ms = __ldcg(base + s * SLOT + DV * BLK_M + r);
+        if (ms == -INFINITY) continue;  // the empty summary: the merge's identity
+        const float ws = exp2f(ms - M);
+        const float* zs = base + s * SLOT + (size_t)(half * HC + 32 * cb) * BLK_M + r;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = fmaf(ws, __ldcg(zs + j * BLK_M), acc[j]);
+      }
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+    uint4* dst = reinterpret_cast<uint4*>(zrow + 32 * cb);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (half * HC + 32 * cb + 8 * j < P.dv)
+        dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  }
+}
+
+template <int DQK, int DV, bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
   using C = ACfg<DQK, DV>;
@@ -329,6 +457,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* o_empty = o_full + 2;           // [2] per tile: z read out by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* split_flag = abort_flag + 1;  // the last split of a tile merges
   // partial row max / row sum exchange between partner softmax threads:
   // [2 halves][2 slots][128 rows] floats
   float* xchg = reinterpret_cast<float*>(bars + 64);
@@ -369,7 +498,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp < 4) {
     if ((warp == 0 || warp == 2) && lane == 0) {
-      produce<C>(P, ring, warp == 0, w);
+      produce<C, SPLIT>(P, ring, warp == 0, w);
     } else if ((warp == 1 || warp == 3) && lane == 0) {
       // Two MMA issuers, one per query tile (warp 1: tile 0, warp 3: tile 1).
       // Each keeps its own short tensor-instruction queue filled, so the
@@ -423,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int i = 0; ok; ++i) {
         const int idx = unit_index(P, i);
         if (idx < 0) break;
-        const Unit u = unit_at(P, idx);
+        const Unit u = unit_at<SPLIT>(P, idx);
         if (u.nmax == 0) continue;
         const int nbt = t ? u.nb1 : u.nb0;
         // the unit's Q tiles are in (this also orders the q_empty arrival
@@ -530,7 +659,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int i = 0;; ++i) {
       const int idx = unit_index(P, i);
       if (idx < 0) break;
-      const Unit u = unit_at(P, idx);
+      const Unit u = unit_at<SPLIT>(P, idx);
       const long long zbase = (long long)u.b * P.n_q * zrow_stride + (long long)u.head * P.dv;
       float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
       for (int kb = 0; kb < u.nmax; ++kb) {
@@ -551,7 +680,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             continue;
           }
           tc_fence_after();
-          const int k0 = kb * BLK_N;
+          const int k0 = (u.kb0 + kb) * BLK_N;
           const bool masked = (k0 + BLK_N > u.L) || (P.causal && k0 + BLK_N - 1 > tq0);
           // allowed keys of this row in this block: k0 + c < lim
           const int lim = (masked ? (P.causal ? min(u.L, q + 1) : u.L) - k0 : BLK_N) - 64 * half;
@@ -648,14 +777,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int q = u.q0 + t * BLK_M + r;
         const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
         __nv_bfloat16* zrow = Zg + zbase + (long long)q * zrow_stride + half * (DV / 2);
-        if (nblk == 0) {
-          // the whole tile is padding: its rows are zero
-          if (q < P.n_q) {
+        if (SPLIT ? !(t ? u.has1 : u.has0) : nblk == 0) {
+          // the whole tile is padding: its rows are zero (written by split 0)
+          if (q < P.n_q && u.split == 0) {
 #pragma unroll
             for (int j = 0; j < DV / 16; ++j)
               if (half * (DV / 2) + 8 * j < P.dv)
                 reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
           }
+          continue;
+        }
+        if (SPLIT) {
+          // publish this split's summary of the tile's rows (the empty
+          // summary when the split holds none of its key blocks)
+          float m_s = -INFINITY, l_s = 0.f;
+          if (nblk > 0) {
+            xch[128 * (xc & 1) + r] = l_run[t];
+            pair_sync();
+            l_s = l_run[t] + pxch[128 * (xc & 1) + r];
+            m_s = m_run[t];
+            ++xc;
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(&o_full[t], (c[t] - 1) & 1, w)))
+              ok = false;
+            if (ok) {
+              tc_fence_after();
+              float* zs = split_slot<DV>(P, u.pidx, t, u.split) + (half * (DV / 2)) * BLK_M + r;
+#pragma unroll
+              for (int cb = 0; cb < DV / 64; ++cb) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + half * (DV / 2) + 32 * cb, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) __stcg(zs + (32 * cb + j) * BLK_M, __uint_as_float(o[j]));
+              }
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&o_empty[t]);
+            }
+          }
+          split_finish<DV>(P, u, t, r, half, m_s, l_s, 9, split_flag);
           continue;
         }
         // the row sum is the two partners' partial sums (same running max)
@@ -741,7 +901,7 @@ struct SpCfg {
   static_assert(STAGES >= 2, "shared memory");
 };
 
-template <int DQK>
+template <int DQK, bool SPLIT>
 __global__ void __launch_bounds__(SP_THREADS, 1)
     attn_tc_sp_kernel(const __grid_constant__ AttnTcParams P) {
   using C = SpCfg<DQK>;
@@ -769,6 +929,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   uint64_t* o_empty = o_full + 2;           // [2] z read out by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* split_flag = abort_flag + 1;  // [2]: the last split of a tile merges
   float* xchg = reinterpret_cast<float*>(bars + 64);
 
   if (threadIdx.x == 0) {
@@ -807,7 +968,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
 
   if (warp < 4) {
     if ((warp == 0 || warp == 2) && lane == 0) {
-      produce<C>(P, ring, warp == 0, w);
+      produce<C, SPLIT>(P, ring, warp == 0, w);
     } else if ((warp == 1 || warp == 3) && lane == 0) {
       // MMA issuer of tile t. Order per tile: S_0, S_1 (once S_0 is read),
       // P_0 V, S_2 (once S_1 is read), P_1 V, ...; S_{j+1} does not wait for
@@ -854,7 +1015,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       for (int i = 0; ok; ++i) {
         const int idx = unit_index(P, i);
         if (idx < 0) break;
-        const Unit u = unit_at(P, idx);
+        const Unit u = unit_at<SPLIT>(P, idx);
         if (u.nmax == 0) continue;
         const int nbt = t ? u.nb1 : u.nb0;
         const int qb = ui % C::Q_BUFS;
@@ -952,7 +1113,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     for (int i = 0;; ++i) {
       const int idx = unit_index(P, i);
       if (idx < 0) break;
-      const Unit u = unit_at(P, idx);
+      const Unit u = unit_at<SPLIT>(P, idx);
       if (t == 1 && !u.pair) continue;  // a single-tile unit: those rows are another unit's
       const int nblk = t ? u.nb1 : u.nb0;
       const int tq0 = u.q0 + t * BLK_M;
@@ -976,7 +1137,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[t]);
-        const int k0 = kb * BLK_N;
+        const int k0 = (u.kb0 + kb) * BLK_N;
         const bool masked = (k0 + BLK_N > u.L) || (P.causal && k0 + BLK_N - 1 > tq0);
         const int lim = (masked ? (P.causal ? min(u.L, q + 1) : u.L) - k0 : BLK_N) - 64 * half;
         if (masked) {
@@ -1050,11 +1211,39 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       // Epilogue of the unit: z / l for this half of each row
       __nv_bfloat16* zrow = Zg + (long long)u.b * P.n_q * zrow_stride + (long long)u.head * DV +
                             (long long)q * zrow_stride + 32 * half;
-      if (nblk == 0) {
-        if (q < P.n_q) {  // the whole tile is padding: its rows are zero
+      if (SPLIT ? !(t ? u.has1 : u.has0) : nblk == 0) {
+        // the whole tile is padding: its rows are zero (written by split 0)
+        if (q < P.n_q && u.split == 0) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
         }
+        continue;
+      }
+      if (SPLIT) {
+        // publish this split's summary of the tile's rows (the empty summary
+        // when the split holds none of its key blocks)
+        float m_s = -INFINITY, l_s = 0.f;
+        if (nblk > 0) {
+          xchg[xo + 128 * (xc & 1)] = l_run;
+          pair_sync();
+          l_s = l_run + xchg[po + 128 * (xc & 1)];
+          m_s = m_run;
+          ++xc;
+          if (ok && !__all_sync(0xffffffffu, mbar_wait(&o_full[t], (cS - 1) & 1, w))) ok = false;
+          if (ok) {
+            tc_fence_after();
+            uint32_t o[32];
+            tmem_ld32(o_addr + 32 * half, o);
+            tmem_wait_ld();
+            float* zs = split_slot<DV>(P, u.pidx, t, u.split) + (32 * half) * BLK_M + r;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) __stcg(zs + j * BLK_M, __uint_as_float(o[j]));
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[t]);
+          }
+        }
+        split_finish<DV>(P, u, t, r, half, m_s, l_s, 9 + t, split_flag + t);
         continue;
       }
       xchg[xo + 128 * (xc & 1)] = l_run;
@@ -1109,10 +1298,14 @@ constexpr double PI_MAJOR_MAX_KV_BYTES = 112.0 * (1 << 20);  // K and V read, ke
 
 // A tile on its own cannot overlap its softmax with its MMAs: a step costs
 // the softmax plus the MMAs, about 1 + 4 (d_h + d_vh) / 1600 pair steps.
+// With a split over the keys a unit also publishes its summaries and may
+// merge them, about SPLIT_FIXED steps.
+constexpr double SPLIT_FIXED = 1.0;
+
 double unit_cost_host(const AttnTcParams& P, int idx, double single_ratio) {
-  int pi, bh, tile;
+  int pi, bh, tile, split, pidx;
   bool pair;
-  unit_coords(P, idx, pi, bh, tile, pair);
+  unit_coords(P, P.nsplit, idx, pi, bh, tile, pair, split, pidx);
   const int b = bh / P.h;
   const int L = P.padding ? P.valid_len[b] : P.n_k;
   const int q_end = P.pad_queries ? (L < P.n_q ? L : P.n_q) : P.n_q;
@@ -1121,10 +1314,12 @@ double unit_cost_host(const AttnTcParams& P, int idx, double single_ratio) {
     if (tq0 >= q_end) return 0;
     int k_end = L;
     if (P.causal && tq0 + BLK_M < k_end) k_end = tq0 + BLK_M;
-    return (k_end + BLK_N - 1) / BLK_N;
+    int kb0;
+    return split_range(P, P.nsplit, (k_end + BLK_N - 1) / BLK_N, split, kb0);
   };
+  const double fixed = P.nsplit > 1 ? SPLIT_FIXED : 0.0;
   if (!pair) return blocks(q0) * single_ratio;
-  return blocks(q0) + (q0 + BLK_M < P.n_q ? blocks(q0 + BLK_M) : 0);
+  return blocks(q0) + (q0 + BLK_M < P.n_q ? blocks(q0 + BLK_M) : 0) + fixed;
 }
 
 // Time of the static schedule of unit_index() on G persistent CTAs.
@@ -1155,14 +1350,56 @@ double per_unit_makespan(const AttnTcParams& P, int G, double sr) {
   return *std::max_element(free_at.begin(), free_at.end());
 }
 
+// Key blocks of n_k keys.
+int key_blocks(int n_k) { return (n_k + BLK_N - 1) / BLK_N; }
+
+// Sets the split over the keys: at most `want` ranges of equal whole blocks
+// (fewer when the blocks do not divide), every unit a tile pair.
+void set_split(AttnTcParams& P, int want) {
+  const int nb = key_blocks(P.n_k);
+  if (want > nb) want = nb;
+  if (want < 2) {
+    P.nsplit = 1;
+    P.split_blocks = nb;
+    return;
+  }
+  P.split_blocks = (nb + want - 1) / want;
+  P.nsplit = (nb + P.split_blocks - 1) / P.split_blocks;
+  if (P.nsplit < 2) P.nsplit = 1;
+  P.pi_major = 0;
+  P.pair_units = P.units = P.npair * P.nbh * P.nsplit;
+}
+
 // Picks one CTA per unit or a persistent grid (and the unit order) for the
-// shorter estimated time on G SMs; returns the grid size.
-int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh, int G) {
+// shorter estimated time on G SMs; returns the grid size. max_split: the
+// largest split over the keys allowed (1: none); a split is considered when
+// the tile pairs alone leave SMs idle, and taken when its estimate is shorter.
+int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh, int G, int max_split) {
   const int pairs = P.npair * P.nbh;
   const double sr = 1.0 + 4.0 * (d_h + d_vh) / 1600.0;
   P.pi_major = 0;
+  P.nsplit = 1;
+  P.split_blocks = key_blocks(P.n_k);
   P.pair_units = P.units = pairs;
-  if (pairs <= G) return pairs;
+  if (pairs <= G) {
+    if (max_split < 2 || 2 * pairs > G) return pairs;
+    // a split over the keys: s ranges per pair, all units in one round
+    const double base = per_unit_makespan(P, G, sr);
+    double best = base;
+    int best_s = 1;
+    for (int s = 2; s <= max_split && (long long)s * pairs <= G; ++s) {
+      AttnTcParams S = P;
+      set_split(S, s);
+      if (S.nsplit < 2) break;
+      const double t = per_unit_makespan(S, G, sr);
+      if (t < best) {
+        best = t;
+        best_s = S.nsplit;
+      }
+    }
+    if (best_s > 1) set_split(P, best_s);
+    return P.units;
+  }
   if (!P.causal && !P.padding) {
     // equal pairs: a persistent grid; the r pairs of a last, partly filled
     // round become 2 r single tiles when that shortens it
@@ -1203,24 +1440,50 @@ int choose_schedule(AttnTcParams& P, int B, int d_h, int d_vh, int G) {
   return best_grid;
 }
 
-template <int DQK, int DV>
-mha_status launch(const AttnTcParams& P, int grid, cudaStream_t s) {
+// A split over the keys fixed by the caller: nsplit ranges (at most one per
+// key block), one CTA per unit, or a persistent grid when there are more
+// units than SMs.
+int forced_split_schedule(AttnTcParams& P, int nsplit, int G) {
+  P.pi_major = 0;
+  P.nsplit = 1;
+  P.split_blocks = key_blocks(P.n_k);
+  P.pair_units = P.units = P.npair * P.nbh;
+  set_split(P, nsplit);
+  return P.units <= G ? P.units : G;
+}
+
+template <int DQK, int DV, bool SPLIT>
+mha_status launch_k(const AttnTcParams& P, int grid, cudaStream_t s) {
   using C = ACfg<DQK, DV>;
-  if (!ensure_smem_limit((const void*)attn_tc_kernel<DQK, DV>, C::SMEM)) return MHA_ERR_CUDA;
-  const cudaError_t e =
-      launch_dependent(attn_tc_kernel<DQK, DV>, dim3(grid), dim3(NTHREADS), C::SMEM, s, P);
+  if (!ensure_smem_limit((const void*)attn_tc_kernel<DQK, DV, SPLIT>, C::SMEM))
+    return MHA_ERR_CUDA;
+  const cudaError_t e = launch_dependent(attn_tc_kernel<DQK, DV, SPLIT>, dim3(grid),
+                                         dim3(NTHREADS), C::SMEM, s, P);
   count_launch();
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
-template <int DQK>
-mha_status launch_sp(const AttnTcParams& P, int grid, cudaStream_t s) {
+template <int DQK, bool SPLIT>
+mha_status launch_sp_k(const AttnTcParams& P, int grid, cudaStream_t s) {
   using C = SpCfg<DQK>;
-  if (!ensure_smem_limit((const void*)attn_tc_sp_kernel<DQK>, C::SMEM)) return MHA_ERR_CUDA;
-  const cudaError_t e =
-      launch_dependent(attn_tc_sp_kernel<DQK>, dim3(grid), dim3(SP_THREADS), C::SMEM, s, P);
+  if (!ensure_smem_limit((const void*)attn_tc_sp_kernel<DQK, SPLIT>, C::SMEM))
+    return MHA_ERR_CUDA;
+  const cudaError_t e = launch_dependent(attn_tc_sp_kernel<DQK, SPLIT>, dim3(grid),
+                                         dim3(SP_THREADS), C::SMEM, s, P);
   count_launch();
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+// The kernels are compiled with and without the split's code, so that a
+// launch without a split runs exactly the unsplit kernel.
+template <int DQK, int DV>
+mha_status launch(const AttnTcParams& P, int grid, cudaStream_t s) {
+  return P.nsplit > 1 ? launch_k<DQK, DV, true>(P, grid, s) : launch_k<DQK, DV, false>(P, grid, s);
+}
+
+template <int DQK>
+mha_status launch_sp(const AttnTcParams& P, int grid, cudaStream_t s) {
+  return P.nsplit > 1 ? launch_sp_k<DQK, true>(P, grid, s) : launch_sp_k<DQK, false>(P, grid, s);
 }
 
 // The units of an attention call: tile pairs of every (batch item, head),
@@ -1242,7 +1505,75 @@ mha_status set_units(AttnTcParams& P, const AttnArgs& a) {
   return MHA_OK;
 }
 
+int split_dv(int d_vh) { return d_vh == 64 ? 64 : 128; }
+
+size_t split_counter_bytes(int pairs) {
+  return ((size_t)pairs * 2 * sizeof(int) + 255) / 256 * 256;
+}
+
+// Largest split the automatic choice considers: all units in one round of at
+// most SPLIT_SM_BOUND SMs (GB300 has 152), at most MAX_SPLITS ranges and one
+// key block per range.
+constexpr int SPLIT_SM_BOUND = 160;
+constexpr int MAX_SPLITS = 64;
+
+int auto_cap(int pairs, int n_k) {
+  if (2 * (long long)pairs > SPLIT_SM_BOUND) return 1;
+  int cap = SPLIT_SM_BOUND / pairs;
+  if (cap > MAX_SPLITS) cap = MAX_SPLITS;
+  if (cap > key_blocks(n_k)) cap = key_blocks(n_k);
+  return cap < 1 ? 1 : cap;
+}
+
+// Resolves the split request of a call: sets the schedule in P and returns
+// the grid, or -1 when a requested split does not fit the scratch.
+int plan_call(AttnTcParams& P, const AttnArgs& a, int G) {
+  const int pairs = P.npair * P.nbh;
+  if (a.nsplit > 1) {
+    const int grid = forced_split_schedule(P, a.nsplit, G);
+    if (P.nsplit > 1 &&
+        (!a.split_ws || a.split_ws_bytes < attention_split_bytes(a.B, a.n_q, a.h, a.d_vh, P.nsplit)))
+      return -1;
+    return grid;
+  }
+  int max_split = 1;
+  if (a.nsplit == 0 && a.split_ws) {
+    max_split = auto_cap(pairs, a.n_k);
+    while (max_split > 1 &&
+           attention_split_bytes(a.B, a.n_q, a.h, a.d_vh, max_split) > a.split_ws_bytes)
+      --max_split;
+  }
+  return choose_schedule(P, a.B, a.d_h, a.d_vh, G, max_split);
+}
+
 }  // namespace
+
+size_t attention_split_bytes(int B, int n_q, int h, int d_vh, int nsplit) {
+  if (nsplit < 2) return 0;
+  const long long pairs = (long long)((n_q + 2 * BLK_M - 1) / (2 * BLK_M)) * h * B;
+  const int dv = split_dv(d_vh);
+  return split_counter_bytes((int)pairs) +
+         (size_t)pairs * 2 * nsplit * (size_t)(dv + 2) * BLK_M * sizeof(float);
+}
+
+size_t attention_split_counter_bytes(int B, int n_q, int h) {
+  return split_counter_bytes((n_q + 2 * BLK_M - 1) / (2 * BLK_M) * h * B);
+}
+
+int attention_effective_splits(int n_k, int nsplit) {
+  const int nb = key_blocks(n_k);
+  if (nsplit > nb) nsplit = nb;
+  if (nsplit < 2) return 1;
+  const int per = (nb + nsplit - 1) / nsplit;
+  const int n = (nb + per - 1) / per;
+  return n < 2 ? 1 : n;
+}
+
+size_t attention_auto_split_bytes(int B, int n_q, int n_k, int h, int d_vh) {
+  const long long pairs = (long long)((n_q + 2 * BLK_M - 1) / (2 * BLK_M)) * h * B;
+  if (2 * pairs > SPLIT_SM_BOUND) return 0;
+  return attention_split_bytes(B, n_q, h, d_vh, auto_cap((int)pairs, n_k));
+}
 
 mha_status attention_tc_plan(const AttnArgs& a, int num_sms, int* grid, int32_t* records,
                              size_t max_records, size_t* n_records) {
@@ -1250,7 +1581,8 @@ mha_status attention_tc_plan(const AttnArgs& a, int num_sms, int* grid, int32_t*
   memset(&P, 0, sizeof(P));
   const mha_status st = set_units(P, a);
   if (st != MHA_OK) return st;
-  const int G = choose_schedule(P, a.B, a.d_h, a.d_vh, num_sms);
+  const int G = plan_call(P, a, num_sms);
+  if (G < 0) return MHA_ERR_WORKSPACE;
   *grid = G;
   size_t n = 0;
   for (int c = 0; c < G; ++c)
@@ -1258,15 +1590,19 @@ mha_status attention_tc_plan(const AttnArgs& a, int num_sms, int* grid, int32_t*
       const int idx = unit_index_of(P, G, c, i);
       if (idx < 0) break;
       if (records && n < max_records) {
-        int pi, bh, tile;
+        int pi, bh, tile, split, pidx;
         bool pair;
-        unit_coords(P, idx, pi, bh, tile, pair);
-        int32_t* r = records + 5 * n;
+        unit_coords(P, P.nsplit, idx, pi, bh, tile, pair, split, pidx);
+        int kb0;
+        const int nkb = split_range(P, P.nsplit, key_blocks(P.n_k), split, kb0);
+        int32_t* r = records + 7 * n;
         r[0] = c;
         r[1] = bh / P.h;
         r[2] = bh % P.h;
         r[3] = pi * 2 * BLK_M + tile * BLK_M;
         r[4] = pair ? 2 : 1;
+        r[5] = kb0 * BLK_N;
+        r[6] = std::min((kb0 + nkb) * BLK_N, P.n_k);
       }
       ++n;
     }
@@ -1306,8 +1642,17 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
   P.has_gate = a.head_gate_host != nullptr && a.h <= MHA_MAX_GATED_HEADS;
   for (int i = 0; i < MHA_MAX_GATED_HEADS; ++i)
     P.head_gate[i] = (P.has_gate && i < a.h) ? a.head_gate_host[i] : 1.f;
-  // one CTA per unit, or one persistent CTA per SM walking its share
-  const int grid = choose_schedule(P, a.B, a.d_h, a.d_vh, num_sms());
+  // one CTA per unit, or one persistent CTA per SM walking its share; a
+  // split over the keys when asked for, or when the tile pairs leave SMs idle
+  const int grid = plan_call(P, a, num_sms());
+  if (grid < 0) return MHA_ERR_WORKSPACE;
+  if (P.nsplit > 1) {
+    const size_t cnt_bytes = split_counter_bytes(P.npair * P.nbh);
+    P.split_cnt = static_cast<int*>(a.split_ws);
+    P.part = reinterpret_cast<float*>(static_cast<char*>(a.split_ws) + cnt_bytes);
+    if (!a.split_cnt_zeroed && cudaMemsetAsync(P.split_cnt, 0, cnt_bytes, s) != cudaSuccess)
+      return MHA_ERR_CUDA;
+  }
   // Head sizes between 64 and 128 run as 128: the 64-wide panels past d_h
   // (past d_vh) are read as zeros (TMA fill past the tensor's extent), so
   // the padded dot products are exact and z's extra columns stay 0 and are

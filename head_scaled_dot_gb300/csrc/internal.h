@@ -67,6 +67,15 @@ struct AttnArgs {
   const int32_t* valid_len_host;  // B entries when padding
   const float* head_gate_host;    // h entries, or null (all 1): head i's output is scaled by it
   int32_t* err;
+  // Split over the keys (tensor-core path): 1 none, 0 automatic (within
+  // split_ws_bytes), n > 1 that many key ranges (fewer when n_k has fewer
+  // 128-key blocks). split_ws: device scratch for the ranges' summaries
+  // (attention_split_bytes), 256-byte aligned, or null; split_cnt_zeroed: the
+  // caller zeroed its first split_counter bytes on the call's stream.
+  int nsplit;
+  void* split_ws;
+  size_t split_ws_bytes;
+  int split_cnt_zeroed;
 };
 
 // Attention of a few query rows over a key/value cache, split over the keys
@@ -112,10 +121,20 @@ mha_status attention_simt(const AttnArgs& a, mha_dtype dt, cudaStream_t s);
 mha_status gemm_tc(const GemmProblem* probs, int nprob, const RowSelect* sel, int32_t* err,
                    cudaStream_t s);
 mha_status attention_tc(const AttnArgs& a, cudaStream_t s);
+// Scratch of a split over the keys into nsplit ranges (0 for nsplit < 2):
+// per-tile counters, then one summary slot per (tile pair, tile, range).
+size_t attention_split_bytes(int B, int n_q, int h, int d_vh, int nsplit);
+// Scratch the automatic split may use for these sizes (0: it never splits).
+size_t attention_auto_split_bytes(int B, int n_q, int n_k, int h, int d_vh);
+// Leading bytes of the split scratch that hold the counters (zeroed per call).
+size_t attention_split_counter_bytes(int B, int n_q, int h);
+// Key ranges a requested split of n_k keys into nsplit ranges gives (1: none).
+int attention_effective_splits(int n_k, int nsplit);
 // The schedule attention_tc would launch on a GPU with num_sms SMs: the grid
 // size and, CTA by CTA in processing order, one record {cta, b, head, q0,
-// ntiles} per unit (query rows [q0, q0 + 128 ntiles) of one head), at most
-// max_records of them written; *n_records = all units. Host only.
+// ntiles, key0, key1} per unit (query rows [q0, q0 + 128 ntiles) of one head
+// over keys [key0, key1)), at most max_records of them written; *n_records =
+// all units. Host only.
 mha_status attention_tc_plan(const AttnArgs& a, int num_sms, int* grid, int32_t* records,
                              size_t max_records, size_t* n_records);
 

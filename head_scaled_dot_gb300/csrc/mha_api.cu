@@ -168,10 +168,14 @@ bool has_padding(mha_mask_kind m) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool tc_head_dims(int d_h, int d_vh);
+
 struct Layout {
-  size_t q, k, v, z, total;
+  size_t q, k, v, z, split, split_bytes, total;
 };
 
+// Error word, Q, K, V, Z, then the scratch of the automatic split over the
+// keys (bf16 heads on the tensor cores whose tile pairs leave SMs idle).
 Layout layout(int B, int n_q, int n_k, int h, int d_h, int d_vh, mha_dtype dt) {
   const size_t es = elem_size(dt);
   Layout L;
@@ -179,7 +183,11 @@ Layout layout(int B, int n_q, int n_k, int h, int d_h, int d_vh, mha_dtype dt) {
   L.k = align_up(L.q + (size_t)B * h * n_q * d_h * es, 1024);
   L.v = align_up(L.k + (size_t)B * h * n_k * d_h * es, 1024);
   L.z = align_up(L.v + (size_t)B * h * n_k * d_vh * es, 1024);
-  L.total = align_up(L.z + (size_t)B * n_q * h * d_vh * es, 1024);
+  L.split = align_up(L.z + (size_t)B * n_q * h * d_vh * es, 1024);
+  L.split_bytes = (dt == MHA_DTYPE_BF16 && tc_head_dims(d_h, d_vh))
+                      ? attention_auto_split_bytes(B, n_q, n_k, h, d_vh)
+                      : 0;
+  L.total = align_up(L.split + L.split_bytes, 1024);
   return L;
 }
 
@@ -276,12 +284,22 @@ mha_status run_out(const void* Z, const void* W_O, void* Y, int B, int n_q, int 
   return gemm_tc(&p, 1, &sel, err, s);
 }
 
+// Split over the keys of one attention call: 1 none, 0 automatic within the
+// scratch, n > 1 n ranges; ws: device scratch (or null); zeroed: its counters
+// were zeroed on the stream by the caller.
+struct SplitReq {
+  int nsplit;
+  void* ws;
+  size_t bytes;
+  int zeroed;
+};
+
 // The attention step with its checks; head_gate (host, h floats) may be null.
 mha_status attention_step(const void* Q, const void* K, const void* V, void* Z, int B, int n_q,
                           int n_k, int h, int d_h, int d_vh, float c, mha_mask_kind mask,
                           const int32_t* valid_len, int self_attention,
                           const float* head_gate, mha_dtype dt, int32_t* dev_error,
-                          void* stream) {
+                          void* stream, SplitReq split = SplitReq{1, nullptr, 0, 0}) {
   if (!Q || !K || !V || !Z) return MHA_ERR_INVALID_ARG;
   if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
     return MHA_ERR_INVALID_ARG;
@@ -316,6 +334,10 @@ mha_status attention_step(const void* Q, const void* K, const void* V, void* Z, 
   a.valid_len_host = valid_len;
   a.head_gate_host = head_gate;
   a.err = dev_error;
+  a.nsplit = split.nsplit;
+  a.split_ws = split.ws;
+  a.split_ws_bytes = split.bytes;
+  a.split_cnt_zeroed = split.zeroed;
   return run_attention(a, dt, static_cast<cudaStream_t>(stream));
 }
 
@@ -383,6 +405,33 @@ mha_status mha_attention(const void* Q, const void* K, const void* V, void* Z, i
                         self_attention, nullptr, dt, dev_error, stream);
 }
 
+size_t mha_attention_split_workspace_size(int B, int n_q, int n_k, int h, int d_h, int d_vh,
+                                          int nsplit) {
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0 || nsplit < 0)
+    return 0;
+  if (!tc_head_dims(d_h, d_vh)) return 0;
+  if (nsplit == 0) return attention_auto_split_bytes(B, n_q, n_k, h, d_vh);
+  return attention_split_bytes(B, n_q, h, d_vh, attention_effective_splits(n_k, nsplit));
+}
+
+mha_status mha_attention_split(const void* Q, const void* K, const void* V, void* Z, int B,
+                               int n_q, int n_k, int h, int d_h, int d_vh, float c,
+                               mha_mask_kind mask, const int32_t* valid_len, int self_attention,
+                               int nsplit, mha_dtype dt, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_error, void* stream) {
+  if (nsplit < 0 || nsplit > MHA_MAX_KEY_SPLITS) return MHA_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MHA_ERR_WORKSPACE;
+  const bool tc = dt == MHA_DTYPE_BF16 && tc_head_dims(d_h, d_vh);
+  if (nsplit > 1 && !tc) return MHA_ERR_UNSUPPORTED;
+  if (nsplit > 1 && n_k > 0 && attention_effective_splits(n_k, nsplit) > 1 &&
+      (!workspace || workspace_bytes < mha_attention_split_workspace_size(
+                                           B, n_q, n_k, h, d_h, d_vh, nsplit)))
+    return MHA_ERR_WORKSPACE;
+  SplitReq split{nsplit, workspace, workspace ? workspace_bytes : 0, 0};
+  return attention_step(Q, K, V, Z, B, n_q, n_k, h, d_h, d_vh, c, mask, valid_len,
+                        self_attention, nullptr, dt, dev_error, stream, split);
+}
+
 mha_status mha_output_projection(const void* Z, const void* W_O, void* Y, int B, int n_q, int h,
                                  int d_vh, int d_o, const int32_t* valid_len, mha_dtype dt,
                                  int32_t* dev_error, void* stream) {
@@ -446,12 +495,21 @@ mha_status mha_forward_general(const void* X_q, const void* X_k, const void* X_v
   void* V = ws + L.v;
   void* Z = ws + L.z;
   if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return MHA_ERR_CUDA;
+  // the split counters are zeroed here, ahead of the projection, so that the
+  // attention kernel still follows the projection kernel directly
+  SplitReq split{0, nullptr, 0, 1};
+  if (L.split_bytes > 0) {
+    split.ws = ws + L.split;
+    split.bytes = L.split_bytes;
+    if (cudaMemsetAsync(split.ws, 0, attention_split_counter_bytes(B, n_q, h), s) != cudaSuccess)
+      return MHA_ERR_CUDA;
+  }
   const int32_t* lens = has_padding(mask) ? valid_len : nullptr;
   st = run_qkv(X_q, X_k, X_v, W_Q, W_K, W_V, Q, K, V, B, n_q, n_k, d_q, d_k, d_v, h, d_h, d_vh,
                lens, self_attention ? 1 : 0, dt, err, s);
   if (st != MHA_OK) return st;
   st = attention_step(Q, K, V, Z, B, n_q, n_k, h, d_h, d_vh, c, mask, valid_len,
-                      self_attention ? 1 : 0, head_gate, dt, err, stream);
+                      self_attention ? 1 : 0, head_gate, dt, err, stream, split);
   if (st != MHA_OK) return st;
   // padded query rows (self-attention) are zeros in Z, so in Y
   return mha_output_projection(Z, W_O, Y, B, n_q, h, d_vh, d_o, self_attention ? lens : nullptr,
@@ -557,9 +615,10 @@ mha_status mha_selftest_wait_timeout(int32_t* dev_error, uint64_t limit_ns, void
 
 mha_status mha_attention_plan(int B, int n_q, int n_k, int h, int d_h, int d_vh,
                               mha_mask_kind mask, const int32_t* valid_len, int self_attention,
-                              int num_sms, int32_t* grid, int32_t* records, size_t max_records,
-                              size_t* n_records) {
+                              int nsplit, int num_sms, int32_t* grid, int32_t* records,
+                              size_t max_records, size_t* n_records) {
   if (!grid || !n_records || num_sms < 1) return MHA_ERR_INVALID_ARG;
+  if (nsplit < 0 || nsplit > MHA_MAX_KEY_SPLITS) return MHA_ERR_INVALID_ARG;
   if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_h <= 0 || d_vh <= 0)
     return MHA_ERR_INVALID_ARG;
   if (!mask_ok(mask)) return MHA_ERR_INVALID_ARG;
@@ -579,6 +638,11 @@ mha_status mha_attention_plan(int B, int n_q, int n_k, int h, int d_h, int d_vh,
   a.padding = has_padding(mask);
   a.pad_queries = has_padding(mask) && self_attention;
   a.valid_len_host = valid_len;
+  // the plan launches nothing: the scratch is only sized, never touched
+  static char no_scratch;
+  a.nsplit = nsplit;
+  a.split_ws_bytes = mha_attention_split_workspace_size(B, n_q, n_k, h, d_h, d_vh, nsplit);
+  a.split_ws = a.split_ws_bytes > 0 ? &no_scratch : nullptr;
   int g = 0;
   const mha_status ps = attention_tc_plan(a, num_sms, &g, records, max_records, n_records);
   *grid = g;

@@ -34,7 +34,8 @@ EXPORTS = (
     "mha_output_projection", "mha_get_device_error", "mha_status_string",
     "mha_selftest_wait_timeout", "mha_kernel_launch_count", "mha_version",
     "mha_forward_no_alloc", "mha_forward_general", "mha_decode_workspace_size",
-    "mha_attention_decode", "mha_attention_plan",
+    "mha_attention_decode", "mha_attention_plan", "mha_attention_split_workspace_size",
+    "mha_attention_split",
 )
 
 _lib = None
@@ -87,7 +88,11 @@ def load(path=LIB_PATH):
     lib.mha_version.restype = ctypes.c_char_p
     lib.mha_version.argtypes = []
     lib.mha_attention_plan.restype = I
-    lib.mha_attention_plan.argtypes = [I] * 6 + [I, P, I, I, P, P, S, P]
+    lib.mha_attention_plan.argtypes = [I] * 6 + [I, P, I, I, I, P, P, S, P]
+    lib.mha_attention_split_workspace_size.restype = S
+    lib.mha_attention_split_workspace_size.argtypes = [I] * 7
+    lib.mha_attention_split.restype = I
+    lib.mha_attention_split.argtypes = [P] * 4 + [I] * 6 + [F, I, P, I, I, I, P, S, P, P]
     _lib = lib
     return lib
 
@@ -139,22 +144,28 @@ def workspace_layout(B, n_q, n_k, h, d_h, d_vh, dtype):
 
 
 def attention_plan(B, n_q, n_k, h, d_h, d_vh, mask="none", valid_len=None,
-                   self_attention=True, num_sms=152):
+                   self_attention=True, num_sms=152, nsplit=1):
     """The tensor-core attention schedule for a GPU with num_sms SMs (host
     only): (grid, records), records an int32 array of rows (cta, b, head, q0,
-    ntiles), CTA by CTA in processing order."""
+    ntiles, key0, key1), CTA by CTA in processing order. nsplit: 1 the
+    schedule of mha_attention, 0 that of mha_forward (automatic split over
+    the keys), n > 1 a split into n key ranges."""
     import numpy as np
     lib = load()
     lens_arg, keep = _lens(valid_len, B)
     grid = ctypes.c_int32()
     n = ctypes.c_size_t()
     args = (B, n_q, n_k, h, d_h, d_vh, MASKS[mask], lens_arg, 1 if self_attention else 0,
-            num_sms, ctypes.byref(grid))
+            int(nsplit), num_sms, ctypes.byref(grid))
     _check(lib.mha_attention_plan(*args, None, 0, ctypes.byref(n)), "mha_attention_plan")
-    rec = (ctypes.c_int32 * (5 * max(1, n.value)))()
+    rec = (ctypes.c_int32 * (7 * max(1, n.value)))()
     _check(lib.mha_attention_plan(*args, rec, n.value, ctypes.byref(n)), "mha_attention_plan")
     del keep
-    return grid.value, np.ctypeslib.as_array(rec).reshape(-1, 5)[:n.value].copy()
+    return grid.value, np.ctypeslib.as_array(rec).reshape(-1, 7)[:n.value].copy()
+
+
+def attention_split_workspace_size(B, n_q, n_k, h, d_h, d_vh, nsplit=0):
+    return int(load().mha_attention_split_workspace_size(B, n_q, n_k, h, d_h, d_vh, int(nsplit)))
 
 
 def launch_count():
@@ -288,6 +299,31 @@ def attention(Q, K, V, c, mask="none", valid_len=None, self_attention=True, out=
                            _ptr(dev_error), _stream(stream))
     del keep
     _check(st, "mha_attention")
+    return out
+
+
+def attention_split(Q, K, V, c, mask="none", valid_len=None, self_attention=True, nsplit=0,
+                    out=None, workspace=None, dev_error=None, stream=None):
+    """mha_attention_split: step 2 with the keys of each query tile cut into
+    nsplit ranges on separate thread blocks, their summaries merged (0: the
+    automatic choice)."""
+    lib = load()
+    B, h, n_q, d_h = Q.shape
+    n_k, d_vh = V.shape[2], V.shape[3]
+    dt = TORCH_DTYPES[Q.dtype]
+    if out is None:
+        out = torch.empty((B, n_q, h * d_vh), dtype=Q.dtype, device=Q.device)
+    if workspace is None:
+        nbytes = attention_split_workspace_size(B, n_q, n_k, h, d_h, d_vh, nsplit)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=Q.device)
+    lens, keep = _lens(valid_len, B)
+    st = lib.mha_attention_split(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, n_q, n_k, h, d_h,
+                                 d_vh, float(c), MASKS[mask], lens, int(bool(self_attention)),
+                                 int(nsplit), DTYPES[dt], _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(dev_error),
+                                 _stream(stream))
+    del keep
+    _check(st, "mha_attention_split")
     return out
 
 

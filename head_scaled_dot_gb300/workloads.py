@@ -70,6 +70,18 @@ GENERAL_DIMS = _w("self_bf16_B4_T1024_d768_h8_dh96_none", 4, 1024, 768, 8, 96, "
                   1 / math.sqrt(96), 6)
 
 
+# Few query rows against many keys (the cross-attention workload's heads with
+# n_q of 64 or 128 and n_k = 32768, 16 (batch item, head) pairs): 16 query
+# tile pairs would fill 16 of the SMs, so the attention step splits the keys
+# over thread blocks and merges the summaries. Seeds 7 and 8.
+LONG_KEYS = [
+    Workload(name="cross_bf16_B2_nq%d_nk32768_d1024_h8_dh128_none" % n_q, B=2, n_q=n_q,
+             n_k=32768, d_model=1024, h=8, d_h=128, d_vh=128, d_o=1024, mask="none",
+             dtype="bf16", cross=True, c=1 / math.sqrt(128), seed=seed)
+    for n_q, seed in ((128, 7), (64, 8))
+]
+
+
 def torch_dtype(dtype):
     return {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
 

@@ -99,11 +99,17 @@ typedef enum { MHA_DTYPE_F32 = 0, MHA_DTYPE_BF16 = 1 } mha_dtype;
 /* Most heads a head gate (mha_forward_general) may address. */
 #define MHA_MAX_GATED_HEADS 1024
 
+/* Largest split over the keys mha_attention_split and mha_attention_plan take. */
+#define MHA_MAX_KEY_SPLITS 256
+
 /*
  * Bytes of device workspace mha_forward needs for these sizes: the head-split
  * Q, K (B*h*n*d_h elements), V (B*h*n_k*d_vh), the concatenated Z
- * (B*n_q*h*d_vh) and a 256-byte header whose first int32 is the device error
- * word. Linear in n_q and n_k: no term grows with n_q * n_k. Returns 0 when an
+ * (B*n_q*h*d_vh), a 256-byte header whose first int32 is the device error
+ * word, and, for bf16 heads on the tensor cores with few query tiles, the
+ * scratch of the automatic split over the keys (see mha_attention_split:
+ * mha_attention_split_workspace_size with nsplit = 0, at most about 21 MB).
+ * Linear in n_q and n_k: no term grows with n_q * n_k. Returns 0 when an
  * argument is non-positive or the dtype is unknown.
  */
 MHA_API size_t mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int d_h,
@@ -113,8 +119,10 @@ MHA_API size_t mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, i
  * Byte offsets inside the workspace of mha_forward, for callers that want to
  * inspect the intermediates or run the three steps themselves on the same
  * buffers: offsets[0] the int32 device error word, [1] Q, [2] K, [3] V, [4] Z,
- * [5] the total size (= mha_workspace_size). Returns MHA_ERR_INVALID_ARG on a
- * non-positive size, an unknown dtype or a NULL `offsets`.
+ * [5] the total size (= mha_workspace_size). The bytes between the end of Z
+ * (rounded up to 1 KB) and the total are the split scratch. Returns
+ * MHA_ERR_INVALID_ARG on a non-positive size, an unknown dtype or a NULL
+ * `offsets`.
  */
 MHA_API mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h, int d_vh,
                                         mha_dtype dt, size_t offsets[6]);
@@ -139,6 +147,9 @@ MHA_API mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h,
  * cores (sizes above 64 in the 128-wide kernels, the columns past d_h or d_vh
  * read as zeros), other sizes on CUDA cores.
  * bf16 also needs d_model, d_h, d_vh and d_o to be multiples of 8.
+ * When the bf16 tile pairs of the attention step are too few to fill the
+ * GPU, the step splits the keys as mha_attention_split does with nsplit = 0,
+ * in the workspace's split scratch (one more small memset, of its counters).
  * Enqueues a 4-byte memset of the error word and three kernels. Everything
  * it enqueues is stream-ordered, so the call can be captured in a CUDA graph
  * on fixed buffers and replayed; host-side arguments (sizes, c, valid_len)
@@ -236,27 +247,77 @@ MHA_API mha_status mha_attention(const void* Q, const void* K, const void* V, vo
                          void* stream);
 
 /*
- * The schedule mha_attention uses for bf16 heads on the tensor cores (d_h
- * and d_vh in 64..128, multiples of 8), computed on the host for a GPU with
- * num_sms SMs;
- * it launches nothing and needs no GPU. A unit is one 128-row query tile or
- * a pair of them, of one (batch item, head); each CTA of the grid takes its
- * units in order. Outputs:
+ * Bytes of device scratch mha_attention_split needs: nsplit = 0 (the
+ * automatic choice) the most it may use for these sizes, 0 when it would
+ * never split; nsplit >= 1 that split (0 for nsplit = 1, or when n_k has a
+ * single 128-key block). The scratch holds one int counter per query tile,
+ * then one summary per (query tile, key range): z (d_vh rounded up to 64 or
+ * 128 columns), m and l of its 128 rows, in fp32. 0 for non-positive sizes
+ * or head sizes outside the tensor-core path.
+ */
+MHA_API size_t mha_attention_split_workspace_size(int B, int n_q, int n_k, int h, int d_h,
+                                                  int d_vh, int nsplit);
+
+/*
+ * Step 2 with the keys of each (query tile, head) cut into ranges that run on
+ * separate thread blocks ("Stable summary of an attention key block",
+ * alphabetamath.cc, Definition: the summary of a union of disjoint key sets
+ * is the merge of their summaries). For few query rows over many keys, such
+ * as a short query block against a long key sequence, the tile pairs alone
+ * would leave most SMs idle. Each range folds its key blocks into its own
+ * summary (m, l, z) of every row and publishes it in the scratch; the thread
+ * block that publishes the last range of a tile merges the tile's summaries
+ * in range order (m' = max m_s, l' = sum e^{m_s - m'} l_s, z' likewise) and
+ * writes z' / l' to Z. No thread block waits for another.
+ *   nsplit      0: automatic (a split only when the tile pairs leave SMs
+ *               idle and the estimate is shorter, within workspace_bytes);
+ *               1: none (as mha_attention); n in 2..MHA_MAX_KEY_SPLITS: the
+ *               128-key blocks of n_k cut into n ranges of equal whole blocks
+ *               (fewer ranges when they do not divide); any mask. A range
+ *               that holds no allowed key of a tile (past a valid length,
+ *               past the causal diagonal) is the empty summary.
+ *   workspace   device scratch of mha_attention_split_workspace_size bytes,
+ *               256-byte aligned, contents on entry irrelevant (its counters
+ *               are zeroed by a memset this call enqueues); may be NULL for
+ *               nsplit 0 or 1
+ * Other arguments as for mha_attention. Errors as for mha_attention, and:
+ * MHA_ERR_INVALID_ARG for nsplit outside [0, MHA_MAX_KEY_SPLITS];
+ * MHA_ERR_UNSUPPORTED for nsplit > 1 with fp32 or head sizes off the tensor
+ * cores; MHA_ERR_WORKSPACE for a missing, misaligned or small workspace.
+ * Calls sharing a workspace must not overlap on the GPU.
+ */
+MHA_API mha_status mha_attention_split(const void* Q, const void* K, const void* V, void* Z,
+                                       int B, int n_q, int n_k, int h, int d_h, int d_vh,
+                                       float c, mha_mask_kind mask, const int32_t* valid_len,
+                                       int self_attention, int nsplit, mha_dtype dt,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_error, void* stream);
+
+/*
+ * The schedule of the tensor-core attention for bf16 heads (d_h and d_vh in
+ * 64..128, multiples of 8), computed on the host for a GPU with num_sms SMs;
+ * it launches nothing and needs no GPU. nsplit as for mha_attention_split:
+ * 1 is the schedule of mha_attention, 0 that of mha_forward (the automatic
+ * split with the scratch mha_workspace_size provides). A unit is one 128-row
+ * query tile or a pair of them, of one (batch item, head), over a range of
+ * keys; each CTA of the grid takes its units in order. Outputs:
  *   *grid        CTAs the launch would use (num_sms for the persistent
  *                schedule, the number of units for one CTA per unit)
- *   records      HOST int32 array of 5 * max_records (may be NULL): for each
+ *   records      HOST int32 array of 7 * max_records (may be NULL): for each
  *                unit, CTA by CTA in processing order, {cta, b, head, q0,
- *                ntiles}: query rows [q0, q0 + 128 ntiles) of head `head` of
- *                batch item b (rows at or past n_q do not exist); at most
+ *                ntiles, key0, key1}: query rows [q0, q0 + 128 ntiles) of
+ *                head `head` of batch item b (rows at or past n_q do not
+ *                exist) over keys [key0, key1) (before the mask); at most
  *                max_records records are written
  *   *n_records   the number of units (records needed)
  * Arguments as for mha_attention; MHA_ERR_INVALID_ARG on a NULL grid or
- * n_records, num_sms < 1 or an invalid size or mask, MHA_ERR_EMPTY_ROW on a
- * bad valid length, MHA_ERR_UNSUPPORTED for other head sizes.
+ * n_records, num_sms < 1, nsplit outside [0, MHA_MAX_KEY_SPLITS] or an
+ * invalid size or mask, MHA_ERR_EMPTY_ROW on a bad valid length,
+ * MHA_ERR_UNSUPPORTED for other head sizes.
  */
 MHA_API mha_status mha_attention_plan(int B, int n_q, int n_k, int h, int d_h, int d_vh,
                               mha_mask_kind mask, const int32_t* valid_len,
-                              int self_attention, int num_sms, int32_t* grid,
+                              int self_attention, int nsplit, int num_sms, int32_t* grid,
                               int32_t* records, size_t max_records, size_t* n_records);
 
 /*

@@ -56,8 +56,13 @@ def test_workspace_size_is_linear_in_sequence_lengths(lib):
     # doubling both lengths at most doubles the bytes (plus alignment): no n_q*n_k term
     assert ws(2048, 2048) <= 2 * base + 4096
     assert ws(8192, 8192) <= 8 * base + 4 * 8192
+    # Q, K, V, Z after the 256-byte header, then the automatic split's scratch
+    # (bounded whatever the lengths: at most 160 query tile pairs' summaries)
+    split = mha.attention_split_workspace_size(2, 1024, 1024, 4, 64, 64, 0)
+    assert 0 < split <= 160 * 2 * 66 * 128 * 4 + 256
     exact = 256 + 2 * 4 * (1024 * 64 * 3 + 1024 * 64) * 2
-    assert exact <= base <= exact + 4 * 1024
+    assert exact + split <= base <= exact + split + 4 * 1024
+    assert mha.workspace_size(2, 1024, 1024, 256, 4, 64, 64, 256, "f32") <= 2 * exact + 4096
     assert mha.workspace_size(0, 1, 1, 1, 1, 1, 1, 1, "bf16") == 0
 
 

@@ -1,8 +1,10 @@
 """The tensor-core attention schedule, checked on the host (no GPU): the
 plan mha_attention would launch (mha_attention_plan) must hand every query
 tile of every (batch item, head) to exactly one CTA, whatever the sizes,
-masks and SM count. A tile handed out twice would be written twice (a race);
-a tile never handed out would leave rows of Z unwritten."""
+masks and SM count, and with a split over the keys every (query tile, key
+block) to exactly one unit. A tile handed out twice would be written twice
+(a race); a tile never handed out would leave rows of Z unwritten; a key
+block in two ranges would be counted twice in the merged summary."""
 
 import numpy as np
 import pytest
@@ -12,24 +14,32 @@ from head_scaled_dot_gb300 import mha
 BLK = 128
 
 
-def check_plan(B, n_q, n_k, h, d, mask, lens, self_attention, sms):
-    grid, rec = mha.attention_plan(B, n_q, n_k, h, d[0], d[1], mask, lens, self_attention, sms)
+def check_plan(B, n_q, n_k, h, d, mask, lens, self_attention, sms, nsplit=1):
+    grid, rec = mha.attention_plan(B, n_q, n_k, h, d[0], d[1], mask, lens, self_attention, sms,
+                                   nsplit=nsplit)
     n_tiles = -(-n_q // BLK)
+    n_blocks = -(-n_k // BLK)
     pairs = B * h * (-(-n_q // (2 * BLK)))
-    assert rec.shape[1] == 5 and len(rec) >= pairs
-    cta, b, head, q0, nt = rec.T
+    assert rec.shape[1] == 7 and len(rec) >= pairs
+    cta, b, head, q0, nt, k0, k1 = rec.T
     # CTA by CTA, every CTA of the grid used, none past it
     assert np.all(np.diff(cta) >= 0)
     assert cta.min() == 0 and cta.max() == grid - 1
     assert len(np.unique(cta)) == grid
-    # each existing query tile of each (b, head) exactly once
+    # key ranges: whole 128-key blocks (the last one ends at n_k)
+    assert np.all(k0 % BLK == 0) and np.all(k0 < k1) and np.all(k1 <= n_k)
+    assert np.all((k1 % BLK == 0) | (k1 == n_k))
+    # each (existing query tile, key block) of each (b, head) exactly once
     assert np.all((q0 % BLK) == 0) and np.all((nt == 1) | (nt == 2))
-    cover = np.zeros((B, h, n_tiles), dtype=np.int64)
-    for k in range(2):
-        t = q0 // BLK + k
-        sel = (nt > k) & (t < n_tiles)
-        np.add.at(cover, (b[sel], head[sel], t[sel]), 1)
+    cover = np.zeros((B, h, n_tiles, n_blocks), dtype=np.int64)
+    for u in range(len(rec)):
+        for k in range(nt[u]):
+            t = q0[u] // BLK + k
+            if t < n_tiles:
+                cover[b[u], head[u], t, k0[u] // BLK:-(-k1[u] // BLK)] += 1
     assert np.all(cover == 1)
+    if nsplit == 1:
+        assert np.all(k0 == 0) and np.all(k1 == n_k)
     # pairs start on even tiles; single tiles come in the two halves of a pair
     assert np.all((q0[nt == 2] // BLK) % 2 == 0)
     singles = rec[nt == 1]
@@ -83,6 +93,78 @@ def test_every_tile_exactly_once(mask, sms):
         check_plan(B, n_q, n_k, h, d, mask, lens, self_attention, sms)
 
 
+def test_few_long_tiles_split_over_the_keys():
+    # 16 heads of one 128-row query tile against 32768 keys: 16 tile pairs
+    # would leave 136 of 152 SMs idle; the keys are cut into nine ranges
+    grid, rec = check_plan(2, 128, 32768, 8, (128, 128), "none", None, False, 152, nsplit=0)
+    assert len(rec) == grid == 16 * 9
+    spans = rec[:, 6] - rec[:, 5]
+    assert spans.max() == 29 * BLK and spans.sum() == 16 * 32768
+    # the schedule mha_attention uses (no scratch) does not split
+    grid1, rec1 = check_plan(2, 128, 32768, 8, (128, 128), "none", None, False, 152, nsplit=1)
+    assert len(rec1) == grid1 == 16
+
+
+@pytest.mark.parametrize("cfg", [
+    (4, 1024, 1024, 12, (64, 64), "none", None, True),
+    (8, 2048, 2048, 16, (64, 64), "causal", None, True),
+    (2, 8192, 8192, 16, (128, 128), "causal_padding", [4290, 7796], True),
+    (16, 512, 4096, 8, (128, 128), "none", None, False)])
+def test_full_workloads_are_not_split(cfg):
+    # enough tile pairs to fill the GPU: the automatic choice keeps every
+    # (query tile, head) on one thread block
+    grid, rec = check_plan(*cfg, 152, nsplit=0)
+    assert np.all(rec[:, 5] == 0) and np.all(rec[:, 6] == cfg[2])
+
+
+@pytest.mark.parametrize("mask", ["none", "causal", "padding", "causal_padding"])
+@pytest.mark.parametrize("nsplit", [0, 2, 3, 7, 64])
+def test_split_covers_every_key_block_once(mask, nsplit):
+    rng = np.random.default_rng(11 + nsplit)
+    for trial in range(12):
+        B = int(rng.choice([1, 2, 3]))
+        h = int(rng.choice([1, 3, 8]))
+        n = int(rng.choice(SIZES))
+        self_attention = bool(rng.integers(2)) or "causal" in mask
+        n_q = n
+        n_k = n if self_attention else int(rng.choice(SIZES + [4000, 9000]))
+        d = [(64, 64), (128, 128), (96, 72)][trial % 3]
+        lens = [int(x) for x in rng.integers(1, n_k + 1, B)] if "padding" in mask else None
+        grid, rec = check_plan(B, n_q, n_k, h, d, mask, lens, self_attention, 152, nsplit)
+        n_blocks = -(-n_k // BLK)
+        if nsplit > 1:
+            # as many equal ranges of whole blocks as asked for (fewer when
+            # the blocks do not divide)
+            per = -(-n_blocks // min(nsplit, n_blocks))
+            want = -(-n_blocks // per)
+            pairs = B * h * (-(-n_q // (2 * BLK)))
+            assert len(rec) == pairs * (want if want > 1 else 1)
+
+
+def test_split_workspace_sizes():
+    # counters (one int per query tile, rounded to 256 bytes), then one slot of
+    # (64 or 128 + 2) x 128 floats per (tile, key range)
+    assert mha.attention_split_workspace_size(2, 128, 32768, 8, 128, 128, 1) == 0
+    assert mha.attention_split_workspace_size(2, 128, 32768, 8, 128, 128, 9) == \
+        256 + 16 * 2 * 9 * 130 * 128 * 4
+    # 8 key blocks asked to make 5 ranges: ranges of 2 blocks, so 4 of them
+    assert mha.attention_split_workspace_size(1, 300, 1000, 2, 64, 64, 5) == \
+        256 + 4 * 2 * 4 * 66 * 128 * 4
+    # more ranges than key blocks: one range per block
+    assert mha.attention_split_workspace_size(1, 128, 300, 1, 64, 64, 50) == \
+        256 + 1 * 2 * 3 * 66 * 128 * 4
+    # the automatic choice: the most it may take, none for full workloads
+    assert mha.attention_split_workspace_size(2, 128, 32768, 8, 128, 128, 0) == \
+        256 + 16 * 2 * 10 * 130 * 128 * 4
+    assert mha.attention_split_workspace_size(8, 2048, 2048, 16, 64, 64, 0) == 0
+    # head sizes off the tensor cores never split
+    assert mha.attention_split_workspace_size(1, 128, 4096, 1, 32, 32, 4) == 0
+    # mha_forward's workspace includes the automatic split's scratch
+    base = mha.workspace_size(2, 128, 32768, 1024, 8, 128, 128, 1024, "f32")
+    assert mha.workspace_size(2, 128, 32768, 1024, 8, 128, 128, 1024, "bf16") >= \
+        base // 2 + mha.attention_split_workspace_size(2, 128, 32768, 8, 128, 128, 0)
+
+
 def test_many_units_run_one_cta_each():
     # more units than the host simulates (65536): one CTA per unit
     grid, rec = check_plan(1024, 1024, 1024, 32, (64, 64), "causal_padding",
@@ -106,3 +188,5 @@ def test_plan_rejects_what_attention_rejects():
     assert status(2, 256, 256, 4, 64, 64, "padding", [0, 10]) == 3    # EMPTY_ROW
     assert status(2, 256, 256, 4, 64, 64, "padding", [10, 257]) == 3
     assert status(1025, 8, 8, 1, 64, 64, "padding", [1] * 1025) == 2  # beyond the length table
+    assert status(2, 256, 256, 4, 64, 64, nsplit=-1) == 1
+    assert status(2, 256, 256, 4, 64, 64, nsplit=257) == 1
