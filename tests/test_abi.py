@@ -139,6 +139,22 @@ def test_steps_reject_bad_arguments_on_host(lib):
     assert lib.mha_selftest_wait_timeout(None, 1000, None) == 1
 
 
+def test_split_attention_rejects_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+
+    def split(nsplit, ws=1 << 20, ws_bytes=1 << 30, dt=1, d=64, n_k=4096, c=0.1, mask=0):
+        return lib.mha_attention_split(P(16), P(32), P(48), P(64), 1, 128, n_k, 2, d, d, c,
+                                       mask, None, 0, nsplit, dt, P(ws) if ws else None,
+                                       ws_bytes, None, None)
+    assert split(-1) == 1 and split(257) == 1                 # INVALID_ARG
+    assert split(4, dt=0) == 2 and split(4, d=32) == 2        # fp32 / off the tensor cores
+    assert split(4, ws=None) == 4                              # WORKSPACE: missing,
+    assert split(4, ws=(1 << 20) + 16) == 4                    # misaligned,
+    assert split(4, ws_bytes=1000) == 4                        # too small
+    assert split(4, c=math.nan) == 1                           # the step's own checks
+    assert split(4, mask=2) == 1                               # padding without lengths
+
+
 def _gen(lib, **kw):
     """mha_forward_general with fake pointers; every call here must be rejected
     by the host checks."""
