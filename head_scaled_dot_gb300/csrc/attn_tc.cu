@@ -109,8 +109,8 @@ struct AttnTcParams {
   float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale, read only when has_gate
 };
 
-// bytes after the K/V ring: barriers (up to 64 x 8 B) and the 2 KB exchange
-constexpr int EXTRA = 512 + 2 * 2 * 128 * 4;
+// bytes after the K/V ring: barriers (up to 64 x 8 B)
+constexpr int EXTRA = 512;
 
 template <int DQK, int DV>
 struct ACfg {
@@ -360,33 +360,33 @@ __device__ __forceinline__ float* split_slot(const AttnTcParams& P, int pidx, in
   return P.part + ((size_t)(pidx * 2 + t) * P.nsplit + s) * (size_t)((DV + 2) * BLK_M);
 }
 
+template <int NTHR>
 __device__ __forceinline__ void tile_sync(int bar_id) {
-  asm volatile("bar.sync %0, 256;" ::"r"(bar_id) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(NTHR) : "memory");
 }
 
-// Called by all 256 softmax threads of tile t (named barrier bar_id) once the
-// thread's half row of z (columns [half DV/2, (half + 1) DV/2)) is in the
-// slot: publishes (m, l) of row r, counts the split, and in the last thread
-// block merges and stores row r's half of Z. flag: one shared int.
-template <int DV>
-__device__ void split_finish(const AttnTcParams& P, const Unit& u, int t, int r, int half,
+// Called by the NTHR threads that hold tile t's rows (named barrier bar_id)
+// once the thread's NC columns [c0, c0 + NC) of row r of z are in the slot:
+// publishes (m, l) of row r, counts the split, and in the last thread block
+// merges and stores those columns of row r of Z. flag: one shared int.
+template <int DV, int NC, int NTHR>
+__device__ void split_finish(const AttnTcParams& P, const Unit& u, int t, int r, int c0,
                              float m, float l, int bar_id, volatile int* flag) {
-  constexpr int HC = DV / 2;
   float* slot = split_slot<DV>(P, u.pidx, t, u.split);
-  if (half == 0) {
+  if (c0 == 0) {
     __stcg(slot + DV * BLK_M + r, m);
     __stcg(slot + (DV + 1) * BLK_M + r, l);
   }
   __threadfence();
-  tile_sync(bar_id);
-  if (r == 0 && half == 0) {
+  tile_sync<NTHR>(bar_id);
+  if (r == 0 && c0 == 0) {
     int* cnt = P.split_cnt + u.pidx * 2 + t;
     const int last = atomicAdd(cnt, 1) == P.nsplit - 1;
     if (last) atomicExch(cnt, 0);  // every split has counted: ready for the next call
     __threadfence();
     *flag = last;
   }
-  tile_sync(bar_id);
+  tile_sync<NTHR>(bar_id);
   if (!*flag) return;
   __threadfence();
   const int q = u.q0 + t * BLK_M + r;
@@ -404,9 +404,9 @@ __device__ void split_finish(const AttnTcParams& P, const Unit& u, int t, int r,
   const float inv = computed ? (P.has_gate ? P.head_gate[u.head] : 1.f) / lsum : 0.f;
   __nv_bfloat16* zrow = static_cast<__nv_bfloat16*>(P.Z) +
                         ((long long)u.b * P.n_q + q) * ((long long)P.h * P.dv) +
-                        (long long)u.head * P.dv + half * HC;
+                        (long long)u.head * P.dv + c0;
 #pragma unroll 1
-  for (int cb = 0; cb < HC / 32; ++cb) {
+  for (int cb = 0; cb < NC / 32; ++cb) {
     float acc[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) acc[j] = 0.f;
@@ -415,7 +415,7 @@ __device__ void split_finish(const AttnTcParams& P, const Unit& u, int t, int r,
         const float ms = __ldcg(base + s * SLOT + DV * BLK_M + r);
         if (ms == -INFINITY) continue;  // the empty summary: the merge's identity
         const float ws = exp2f(ms - M);
-        const float* zs = base + s * SLOT + (size_t)(half * HC + 32 * cb) * BLK_M + r;
+        const float* zs = base + s * SLOT + (size_t)(c0 + 32 * cb) * BLK_M + r;
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = fmaf(ws, __ldcg(zs + j * BLK_M), acc[j]);
       }
@@ -426,7 +426,7 @@ __device__ void split_finish(const AttnTcParams& P, const Unit& u, int t, int r,
     uint4* dst = reinterpret_cast<uint4*>(zrow + 32 * cb);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      if (half * HC + 32 * cb + 8 * j < P.dv)
+      if (c0 + 32 * cb + 8 * j < P.dv)
         dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
   }
 }
@@ -458,9 +458,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* split_flag = abort_flag + 1;  // the last split of a tile merges
-  // partial row max / row sum exchange between partner softmax threads:
-  // [2 halves][2 slots][128 rows] floats
-  float* xchg = reinterpret_cast<float*>(bars + 64);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -632,30 +629,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     // Softmax: warps 4..11 take tile 0 then tile 1 for every key block, so
     // the two tiles' softmaxes alternate (they share the exponential units)
-    // and each overlaps the other tile's MMAs. A row is split between the
-    // two warps that see the same TMEM lane slice (w and w + 4): `half`
-    // selects key columns [64 half, 64 half + 64) of S and value columns
-    // [half DV/2, (half + 1) DV/2) of z. The partners combine their partial
-    // row max through shared memory (a 64-thread named barrier) and keep
-    // partial row sums, added once at the end of a unit.
-    const int g = warp & 3;           // TMEM lane slice 32*g .. 32*g+31
-    const int half = (warp - 4) >> 2;  // 0: warps 4..7, 1: warps 8..11
-    const int r = 32 * g + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * g) << 16;
+    // and each overlaps the other tile's MMAs. A warp holds 16 rows, lanes i
+    // and i + 16 the two halves of row 32 g + 16 hh + i (`half` = lane / 16:
+    // key columns [64 half, 64 half + 64) of S, value columns
+    // [half DV/2, (half + 1) DV/2) of z), read and written with the
+    // half-split TMEM shape; the partners combine their partial row maximum
+    // with a shuffle and keep partial row sums, added once at the end of a
+    // unit. Both halves of a row come in with the same load, so P may
+    // overwrite the first columns of S as soon as that load is waited for.
+    const int g = warp & 3;            // TMEM lane slice 32*g .. 32*g+31
+    const int hh = (warp - 4) >> 2;    // 0: lanes 32g .. 32g+15, 1: lanes 32g+16 .. 32g+31
+    const int half = lane >> 4;
+    const int r = 32 * g + 16 * hh + (lane & 15);
+    const uint32_t lane_off = static_cast<uint32_t>(32 * g + 16 * hh) << 16;
     const float cl2 = P.cl2;
     const float2 cl2x2 = make_float2(cl2, cl2);
-    float* xch = xchg + 2 * 128 * half;        // this thread's slots: [2][128]
-    const float* pxch = xchg + 2 * 128 * (1 - half);  // the partner's
-    auto pair_sync = [&]() {
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + g) : "memory");
-    };
     uint32_t c[2] = {0, 0};  // blocks folded per tile so far (s/p/o_full phases)
-    int xc = 0;              // exchanges so far (alternates the shared slots)
     bool ok = true;
-    // Every (block, tile) step and every tile epilogue below runs exactly one
-    // pair barrier on both partners, whatever happened before (a partner that
-    // gave up on a wait still takes part), so the named barriers can never be
-    // left waiting.
     for (int i = 0;; ++i) {
       const int idx = unit_index(P, i);
       if (idx < 0) break;
@@ -666,17 +656,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int nblk = t ? u.nb1 : u.nb0;
-          if (kb >= nblk) continue;  // uniform across the pair
+          if (kb >= nblk) continue;  // uniform across the warp
           const int tq0 = u.q0 + t * BLK_M;
           const int q = tq0 + r;
           const uint32_t s_addr = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
           const uint32_t o_addr = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
           const uint32_t cc = c[t]++;
           if (ok && !mbar_wait(&s_full[t], cc & 1, w)) ok = false;
-          if (!__all_sync(0xffffffffu, ok)) {  // keep the pair in step, do no work
+          if (!__all_sync(0xffffffffu, ok)) {  // do no work
             ok = false;
-            pair_sync();
-            ++xc;
             continue;
           }
           tc_fence_after();
@@ -685,8 +673,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // allowed keys of this row in this block: k0 + c < lim
           const int lim = (masked ? (P.causal ? min(u.L, q + 1) : u.L) - k0 : BLK_N) - 64 * half;
           uint32_t sr[64];
-          tmem_ld32(s_addr + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-          tmem_ld32(s_addr + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          tmem_ld_x2_64<64>(s_addr, sr);
           tmem_wait_ld();
           if (masked) {
             // forbidden keys get s = -inf, hence weight 2^{-inf} = 0 exactly
@@ -696,12 +683,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int j = 0; j < 64; ++j)
               if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
           }
-          // combine with the partner's half of the row; after this barrier both
-          // halves of S are in registers, so P may overwrite its columns
-          xch[128 * (xc & 1) + r] = max64(sr);
-          pair_sync();
-          const float mx = fmaxf(xch[128 * (xc & 1) + r], pxch[128 * (xc & 1) + r]);
-          ++xc;
+          const float mh = max64(sr);
+          const float mx = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));
           const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
           // raise the running max only past the threshold (or on the first block)
           const bool raise =
@@ -711,30 +694,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const float alpha = ex2_approx(m_run[t] - m_use);  // e^{m - m'}: 1 when m is kept
           const float2 negm = make_float2(-m_use, -m_use);
           float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
-          // p = 2^{c log2(e) s - m} as bf16 into this half's P columns
-          // [32 half, 32 half + 32) of S (two bf16 per column)
+          // p = 2^{c log2(e) s - m} as bf16 over the first 64 columns of S:
+          // this half's keys go to P columns [32 half, 32 half + 32)
+          uint32_t pk[32];
 #pragma unroll
-          for (int cb = 0; cb < 64; cb += 32) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              float2 x0 = __ffma2_rn(
-                  make_float2(__uint_as_float(sr[cb + j]), __uint_as_float(sr[cb + j + 1])),
-                  cl2x2, negm);
-              float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[cb + j + 2]),
-                                                 __uint_as_float(sr[cb + j + 3])),
-                                     cl2x2, negm);
-              x0.x = ex2_approx(x0.x);
-              x0.y = ex2_approx(x0.y);
-              x1.x = ex2_approx(x1.x);
-              x1.y = ex2_approx(x1.y);
-              sum = __fadd2_rn(sum, x0);
-              sum_b = __fadd2_rn(sum_b, x1);
-              pk[j / 2] = pack_bf16x2(x0.x, x0.y);
-              pk[j / 2 + 1] = pack_bf16x2(x1.x, x1.y);
-            }
-            tmem_st16(s_addr + 32 * half + cb / 2, pk);
+          for (int j = 0; j < 64; j += 4) {
+            float2 x0 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])), cl2x2, negm);
+            float2 x1 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3])), cl2x2,
+                negm);
+            x0.x = ex2_approx(x0.x);
+            x0.y = ex2_approx(x0.y);
+            x1.x = ex2_approx(x1.x);
+            x1.y = ex2_approx(x1.y);
+            sum = __fadd2_rn(sum, x0);
+            sum_b = __fadd2_rn(sum_b, x1);
+            pk[j / 2] = pack_bf16x2(x0.x, x0.y);
+            pk[j / 2 + 1] = pack_bf16x2(x1.x, x1.y);
           }
+          tmem_st_x2_32<32>(s_addr, pk);
           l_run[t] = l_run[t] * alpha + ((sum.x + sum.y) + (sum_b.x + sum_b.y));
           // merge: rescale this row of z by e^{m - m'} when m was raised; z must
           // already hold every earlier block (wait for the previous z += P V)
@@ -747,8 +726,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int cb = 0; cb < DV / 64; ++cb) {
               uint32_t o[32];
-              const uint32_t oa = o_addr + half * (DV / 2) + 32 * cb;
-              tmem_ld32(oa, o);
+              const uint32_t oa = o_addr + 32 * cb;
+              tmem_ld_x2_32<DV / 2>(oa, o);
               tmem_wait_ld();
 #pragma unroll
               for (int j = 0; j < 32; j += 2) {
@@ -758,7 +737,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 o[j] = __float_as_uint(v.x);
                 o[j + 1] = __float_as_uint(v.y);
               }
-              tmem_st32(oa, o);
+              tmem_st_x2_32<DV / 2>(oa, o);
             }
           }
           m_run[t] = m_new;
@@ -787,16 +766,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           continue;
         }
+        // the row sum is the two partners' partial sums (same running max)
+        const float l_tot = l_run[t] + __shfl_xor_sync(0xffffffffu, l_run[t], 16);
         if (SPLIT) {
           // publish this split's summary of the tile's rows (the empty
           // summary when the split holds none of its key blocks)
           float m_s = -INFINITY, l_s = 0.f;
           if (nblk > 0) {
-            xch[128 * (xc & 1) + r] = l_run[t];
-            pair_sync();
-            l_s = l_run[t] + pxch[128 * (xc & 1) + r];
+            l_s = l_tot;
             m_s = m_run[t];
-            ++xc;
             if (ok && !__all_sync(0xffffffffu, mbar_wait(&o_full[t], (c[t] - 1) & 1, w)))
               ok = false;
             if (ok) {
@@ -805,7 +783,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
               for (int cb = 0; cb < DV / 64; ++cb) {
                 uint32_t o[32];
-                tmem_ld32(o_addr + half * (DV / 2) + 32 * cb, o);
+                tmem_ld_x2_32<DV / 2>(o_addr + 32 * cb, o);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) __stcg(zs + (32 * cb + j) * BLK_M, __uint_as_float(o[j]));
@@ -815,14 +793,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               if (lane == 0) mbar_arrive(&o_empty[t]);
             }
           }
-          split_finish<DV>(P, u, t, r, half, m_s, l_s, 9, split_flag);
+          split_finish<DV, DV / 2, 256>(P, u, t, r, half * (DV / 2), m_s, l_s, 9, split_flag);
           continue;
         }
-        // the row sum is the two partners' partial sums (same running max)
-        xch[128 * (xc & 1) + r] = l_run[t];
-        pair_sync();
-        const float l_tot = l_run[t] + pxch[128 * (xc & 1) + r];
-        ++xc;
         if (!ok || !__all_sync(0xffffffffu, mbar_wait(&o_full[t], (c[t] - 1) & 1, w))) {
           ok = false;
           continue;
@@ -833,7 +806,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int cb = 0; cb < DV / 64; ++cb) {
           uint32_t o[32];
-          tmem_ld32(o_addr + half * (DV / 2) + 32 * cb, o);
+          tmem_ld_x2_32<DV / 2>(o_addr + 32 * cb, o);
           tmem_wait_ld();
           if (q < P.n_q) {
             uint32_t pk[16];
@@ -886,8 +859,8 @@ struct SpCfg {
   static constexpr int K_BYTES = BLK_N * DQK * 2;
   static constexpr int V_BYTES = BLK_N * 64 * 2;
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-  // barriers (up to 64 x 8 B), then the exchange [2 tiles][2 halves][2 slots][128]
-  static constexpr int EXTRA_SP = 512 + 2 * 2 * 2 * 128 * 4;
+  // barriers (up to 64 x 8 B)
+  static constexpr int EXTRA_SP = 512;
   // a second pair of Q tiles (the next unit's, loaded while the current one
   // runs) where it leaves the ring at four stages
   static constexpr int Q_BUFS =
@@ -930,7 +903,6 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* split_flag = abort_flag + 1;  // [2]: the last split of a tile merges
-  float* xchg = reinterpret_cast<float*>(bars + 64);
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < C::Q_BUFS; ++b) {
@@ -1087,28 +1059,24 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       }
     }
   } else {
-    // Softmax: warps 4..11 own tile 0, warps 12..19 tile 1. A row is split
-    // between the two warps of its tile that see the same TMEM lane slice
-    // (`half`: key columns [64 half, 64 half + 64) of S, z columns
-    // [32 half, 32 half + 32)); the partners combine their partial row max
-    // through shared memory under a 64-thread named barrier.
+    // Softmax: warps 4..11 own tile 0, warps 12..19 tile 1. A warp holds 16
+    // rows of its tile, lanes i and i + 16 the two halves of row
+    // 32 g + 16 hh + i (`half` = lane / 16: key columns [64 half, 64 half + 64)
+    // of S, P columns [32 half, 32 half + 32), z columns [32 half,
+    // 32 half + 32)), read and written with the half-split TMEM shape; the
+    // partners combine their partial row maximum and row sum with a shuffle.
     const int t = (warp - 4) >> 3;
-    const int half = ((warp - 4) >> 2) & 1;
+    const int hh = ((warp - 4) >> 2) & 1;
     const int g = warp & 3;  // TMEM lane slice 32*g .. 32*g+31
-    const int r = 32 * g + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * g) << 16;
+    const int half = lane >> 4;
+    const int r = 32 * g + 16 * hh + (lane & 15);
+    const uint32_t lane_off = static_cast<uint32_t>(32 * g + 16 * hh) << 16;
     const uint32_t s_addr = tmem + lane_off + C::S_COL + 128 * t;
     const uint32_t p_addr = tmem + lane_off + C::P_COL + 64 * t;
     const uint32_t o_addr = tmem + lane_off + C::O_COL + 64 * t;
     const float cl2 = P.cl2;
     const float2 cl2x2 = make_float2(cl2, cl2);
-    const int xo = 256 * (2 * t + half) + r;      // this thread's exchange slots
-    const int po = 256 * (2 * t + 1 - half) + r;  // the partner's
-    auto pair_sync = [&]() {
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + 4 * t + g) : "memory");
-    };
     uint32_t cS = 0;  // blocks of this tile folded so far (s_full / s_free / p_full / o_full)
-    int xc = 0;       // exchanges so far (alternates the shared slots)
     bool ok = true;
     for (int i = 0;; ++i) {
       const int idx = unit_index(P, i);
@@ -1122,16 +1090,13 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       for (int kb = 0; kb < nblk; ++kb) {
         const uint32_t cc = cS++;
         if (ok && !mbar_wait(&s_full[t], cc & 1, w)) ok = false;
-        if (!__all_sync(0xffffffffu, ok)) {  // keep the pair in step, do no work
+        if (!__all_sync(0xffffffffu, ok)) {  // do no work
           ok = false;
-          pair_sync();
-          ++xc;
           continue;
         }
         tc_fence_after();
         uint32_t sr[64];
-        tmem_ld32(s_addr + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(s_addr + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld_x2_64<64>(s_addr, sr);
         tmem_wait_ld();
         // S is in registers: the tile's next S may be computed into its columns
         tc_fence_before();
@@ -1146,10 +1111,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           for (int j = 0; j < 64; ++j)
             if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
         }
-        xchg[xo + 128 * (xc & 1)] = max64(sr);
-        pair_sync();
-        const float mx = fmaxf(xchg[xo + 128 * (xc & 1)], xchg[po + 128 * (xc & 1)]);
-        ++xc;
+        const float mh = max64(sr);
+        const float mx = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));
         const float m_blk = (mx == -INFINITY) ? -INFINITY : mx * cl2;
         // raise the running max only past the threshold (or on the first block)
         const bool raise = (m_run == -INFINITY) ? true : (m_blk > m_run + RESCALE_LOG2);
@@ -1157,7 +1120,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = ex2_approx(m_run - m_use);  // e^{m - m'}: 1 when m is kept
         const float2 negm = make_float2(-m_use, -m_use);
-        // p = 2^{c log2(e) s - m}, all 64 of this half row into registers
+        // p = 2^{c log2(e) s - m}, this half row of 64 into registers
         float2 sum = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
         uint32_t pk[32];
 #pragma unroll
@@ -1185,12 +1148,11 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           }
           tc_fence_after();
         }
-        tmem_st16(p_addr + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(p_addr + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        tmem_st_x2_32<32>(p_addr, pk);
         if (__any_sync(0xffffffffu, kb > 0 && raise)) {
           // merge: rescale this half row of z by e^{m - m'}
           uint32_t o[32];
-          tmem_ld32(o_addr + 32 * half, o);
+          tmem_ld_x2_32<32>(o_addr, o);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
@@ -1200,7 +1162,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
             o[j] = __float_as_uint(v.x);
             o[j + 1] = __float_as_uint(v.y);
           }
-          tmem_st32(o_addr + 32 * half, o);
+          tmem_st_x2_32<32>(o_addr, o);
         }
         m_run = m_new;
         tmem_wait_st();
@@ -1219,21 +1181,20 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         }
         continue;
       }
+      // the row sum is the two partners' partial sums (same running max)
+      const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
       if (SPLIT) {
         // publish this split's summary of the tile's rows (the empty summary
         // when the split holds none of its key blocks)
         float m_s = -INFINITY, l_s = 0.f;
         if (nblk > 0) {
-          xchg[xo + 128 * (xc & 1)] = l_run;
-          pair_sync();
-          l_s = l_run + xchg[po + 128 * (xc & 1)];
+          l_s = l_tot;
           m_s = m_run;
-          ++xc;
           if (ok && !__all_sync(0xffffffffu, mbar_wait(&o_full[t], (cS - 1) & 1, w))) ok = false;
           if (ok) {
             tc_fence_after();
             uint32_t o[32];
-            tmem_ld32(o_addr + 32 * half, o);
+            tmem_ld_x2_32<32>(o_addr, o);
             tmem_wait_ld();
             float* zs = split_slot<DV>(P, u.pidx, t, u.split) + (32 * half) * BLK_M + r;
 #pragma unroll
@@ -1243,13 +1204,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
             if (lane == 0) mbar_arrive(&o_empty[t]);
           }
         }
-        split_finish<DV>(P, u, t, r, half, m_s, l_s, 9 + t, split_flag + t);
+        split_finish<DV, 32, 256>(P, u, t, r, 32 * half, m_s, l_s, 9 + t, split_flag + t);
         continue;
       }
-      xchg[xo + 128 * (xc & 1)] = l_run;
-      pair_sync();
-      const float l_tot = l_run + xchg[po + 128 * (xc & 1)];
-      ++xc;
       if (!ok || !__all_sync(0xffffffffu, mbar_wait(&o_full[t], (cS - 1) & 1, w))) {
         ok = false;
         continue;
@@ -1258,7 +1215,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       const bool computed = q < u.q_end;
       const float inv = computed ? (P.has_gate ? P.head_gate[u.head] : 1.f) / l_tot : 0.f;
       uint32_t o[32];
-      tmem_ld32(o_addr + 32 * half, o);
+      tmem_ld_x2_32<32>(o_addr, o);
       tmem_wait_ld();
       if (q < P.n_q) {
         uint32_t pk[16];
@@ -1485,6 +1442,8 @@ template <int DQK>
 mha_status launch_sp(const AttnTcParams& P, int grid, cudaStream_t s) {
   return P.nsplit > 1 ? launch_sp_k<DQK, true>(P, grid, s) : launch_sp_k<DQK, false>(P, grid, s);
 }
+
+
 
 // The units of an attention call: tile pairs of every (batch item, head),
 // with the lengths the masks use. Host only, no device work.
