@@ -50,6 +50,9 @@ struct DecodeParams {
   // batch item by batch item; item_start[b] = first item of batch item b
   int nitems;
   int item_start[MHA_MAX_PADDED_BATCH + 1];
+  // summaries per DEC_CHUNK keys: DEC_WARPS (one per warp of pass 1), or 1
+  // (the streaming kernel combines its warps' summaries of a chunk first)
+  int per_chunk;
   uint64_t limit_ns;  // bounded waits give up after this long
 };
 
@@ -477,7 +480,11 @@ struct DsCfg {
   static constexpr int ROW = D * 2;               // bytes of one K or V row
   static constexpr int STAGE = 2 * 32 * ROW;      // K rows then V rows of a group
   static constexpr int Q_FLOATS = NQ * D;         // one item's rows, fp32, pre-scaled
-  static constexpr int SMEM = DS_STAGES * STAGE + 2 * Q_FLOATS * 4 + 2 * DS_STAGES * 8 + 16;
+  // the combine of the warps' summaries of a chunk: m and l of each warp,
+  // then each warp's weighted z
+  static constexpr int COMBINE_FLOATS = 2 * DS_WARPS + DS_WARPS * D;
+  static constexpr int SMEM =
+      DS_STAGES * STAGE + 2 * Q_FLOATS * 4 + 2 * DS_STAGES * 8 + 16 + COMBINE_FLOATS * 4;
 };
 
 // Batch item, head and chunk of work item `it`.
@@ -518,6 +525,9 @@ __global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
   uint64_t* full = reinterpret_cast<uint64_t*>(qs + 2 * C::Q_FLOATS);
   uint64_t* empty = full + DS_STAGES;
   int* abort_flag = reinterpret_cast<int*>(empty + DS_STAGES);
+  float* cm = reinterpret_cast<float*>(abort_flag + 4);  // [DS_WARPS] m of each warp
+  float* cl = cm + DS_WARPS;                           // [DS_WARPS] l of each warp
+  float* cz = cl + DS_WARPS;                           // [DS_WARPS][D] weighted z
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < DS_STAGES; ++s) {
@@ -528,6 +538,9 @@ __global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
     fence_mbar_init();
   }
   __syncthreads();
+  // the merge kernel may be launched now: its CTAs wait in grid_dep_wait
+  // until this grid has completed and its summaries are visible
+  grid_dep_launch_dependents();
   const WaitCtl w{nullptr, abort_flag, P.limit_ns};
   const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(P.K);
   const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(P.V);
@@ -685,18 +698,51 @@ __global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
       }
-      // this warp's summaries of the item's rows (empty if it took no group)
+      // The item's summary of each row: the merge of the warps' summaries
+      // (those that took no group are empty), combined through shared memory,
+      // one per chunk. Split `chunk` of the row.
+#pragma unroll 1
+      for (int r = 0; r < P.n_q && r < NQ; ++r) {
+        constexpr int NT = 32 * DS_WARPS;
+        float mr = m_run[0], lr = l_run[0];
 #pragma unroll
-      for (int r = 0; r < NQ; ++r) {
-        if (r >= P.n_q) continue;
-        float* dst = P.part + ((bh * P.n_q + r) * P.nsplit + chunk * DS_WARPS + warp) *
-                                  (long long)(2 + D);
+        for (int rr = 1; rr < NQ; ++rr)
+          if (rr == r) {
+            mr = m_run[rr];
+            lr = l_run[rr];
+          }
         if (lane == 0) {
-          dst[0] = m_run[r];
-          dst[1] = l_run[r];
+          cm[warp] = mr;
+          cl[warp] = lr;
         }
+        asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+        float M = cm[0];
 #pragma unroll
-        for (int t = 0; t < CPL; ++t) dst[2 + lane * CPL + t] = z_run[r][t];
+        for (int i = 1; i < DS_WARPS; ++i) M = fmaxf(M, cm[i]);
+        const float wgt = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+#pragma unroll
+        for (int rr = 0; rr < NQ; ++rr)
+          if (rr == r) {
+#pragma unroll
+            for (int t = 0; t < CPL; ++t) cz[warp * D + lane * CPL + t] = z_run[rr][t] * wgt;
+          }
+        asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+        float* dst = P.part + ((bh * P.n_q + r) * P.nsplit + chunk) * (long long)(2 + D);
+        for (int c = threadIdx.x; c < D; c += NT) {
+          float zc = 0.f;
+#pragma unroll
+          for (int i = 0; i < DS_WARPS; ++i) zc += cz[i * D + c];
+          dst[2 + c] = zc;
+        }
+        if (threadIdx.x == 0) {
+          float l = 0.f;
+#pragma unroll
+          for (int i = 0; i < DS_WARPS; ++i)
+            if (cm[i] != -INFINITY) l += exp2f(cm[i] - M) * cl[i];
+          dst[0] = M;
+          dst[1] = l;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");  // cm, cl, cz free again
       }
     }
   }
@@ -710,9 +756,12 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_merge_kernel(
   __shared__ float w[1024];
   __shared__ float red[DEC_WARPS];
   __shared__ float bcast;
+  // launched as a dependent of pass 1 (programmatic stream serialization):
+  // its summaries are complete and visible once this returns
+  grid_dep_wait();
   const int row = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
   const int L = P.valid_len[b];
-  const int nsp = ((L + DEC_CHUNK - 1) / DEC_CHUNK) * DEC_WARPS;
+  const int nsp = ((L + DEC_CHUNK - 1) / DEC_CHUNK) * P.per_chunk;
   const int dv = P.d_vh;
   const long long bh = (long long)b * P.h + head;
   const float* src = P.part + (bh * P.n_q + row) * P.nsplit * (long long)(2 + dv);
@@ -829,11 +878,13 @@ mha_status launch_decode(DecodeParams& P, int nchunk, cudaStream_t s) {
     if (items < (1ll << 30)) {
       P.item_start[P.B] = (int)items;
       P.nitems = (int)items;
+      P.per_chunk = 1;  // the streaming kernel writes one summary per chunk
       const bool ok = P.d_h == 64 ? launch_stream_rows<64>(P, s) : launch_stream_rows<128>(P, s);
       if (!ok) return MHA_ERR_CUDA;
-      decode_merge_kernel<T><<<g2, DEC_THREADS, 0, s>>>(P);
+      // the merge follows pass 1 without a launch gap
+      const cudaError_t e = launch_dependent(decode_merge_kernel<T>, g2, dim3(DEC_THREADS), 0, s, P);
       count_launch(2);
-      return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+      return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
     }
   }
   if (launch_fast<T, 64, 64>(P, g1, s) || launch_fast<T, 128, 128>(P, g1, s)) {
@@ -882,6 +933,7 @@ mha_status attention_decode(const DecodeArgs& a, mha_dtype dt, cudaStream_t s) {
   P.d_h = a.d_h;
   P.d_vh = a.d_vh;
   P.nsplit = nchunk * DEC_WARPS;
+  P.per_chunk = DEC_WARPS;
   P.cl2 = a.c * 1.4426950408889634f;
   P.causal_tail = a.causal_tail;
   P.limit_ns = wait_limit_ns();
