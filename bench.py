@@ -576,30 +576,30 @@ def run_ours(args):
                                "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
                                "kernels": kr, "roofline": roofline(wj, kr, pk, pk_kind, dev)}
             del r
-        # a general head size (d_h = 96): bf16 heads of 64..128 run in the
-        # 128-wide tensor-core kernels, others on the CUDA cores (against the
-        # fp32 FMA peak); the flop count uses the head size itself
-        gw = workloads.GENERAL_DIMS
-        r = measure_workload(gw, max(3, args.steps // 2), 3, dev, 1, e2e=False,
-                             sample_clocks=False)
-        kr = kernel_rows(r, pk)
-        on_tc = gw.dtype == "bf16" and all(64 <= d <= 128 and d % 8 == 0
-                                           for d in (gw.d_h, gw.d_vh))
-        if on_tc:
-            groof = {"kernel": "attention (tensor cores, head padded to 128)",
-                     "bound": "tensor", "peak": pk["bf16_tflops"],
-                     "peak_kind": pk_kind + " burst"}
-        else:
-            groof = {"kernel": "attention (CUDA cores)", "bound": "alu",
-                     "peak": alu_peak_tflops(dev, sm_max_mhz()),
-                     "peak_kind": "derived: SMs x 128 FP32 lanes x 2 flop x max SM clock"}
-        groof.update(achieved=kr["attention"]["tflops"], unit="TFLOP/s",
-                     frac=kr["attention"]["tflops"] / groof["peak"])
-        others[gw.name] = {"tflops": r["flops"]["total"] * len(r["per"]["step"])
-                           / (r["total_ms"] * 1e-3) / 1e12,
-                           "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
-                           "kernels": kr, "roofline": groof}
-        del r
+        # general head sizes: d_h = 96 (bf16 heads of 64..128 run in the
+        # 128-wide tensor-core kernels) and d_h = 32 (the CUDA-core kernel,
+        # against the fp32 FMA peak); the flop count uses the head size itself
+        for gw in (workloads.GENERAL_DIMS, workloads.SIMT_DIMS):
+            r = measure_workload(gw, max(3, args.steps // 2), 3, dev, 1, e2e=False,
+                                 sample_clocks=False)
+            kr = kernel_rows(r, pk)
+            on_tc = gw.dtype == "bf16" and all(64 <= d <= 128 and d % 8 == 0
+                                               for d in (gw.d_h, gw.d_vh))
+            if on_tc:
+                groof = {"kernel": "attention (tensor cores, head padded to 128)",
+                         "bound": "tensor", "peak": pk["bf16_tflops"],
+                         "peak_kind": pk_kind + " burst"}
+            else:
+                groof = {"kernel": "attention (CUDA cores)", "bound": "alu",
+                         "peak": alu_peak_tflops(dev, sm_max_mhz()),
+                         "peak_kind": "derived: SMs x 128 FP32 lanes x 2 flop x max SM clock"}
+            groof.update(achieved=kr["attention"]["tflops"], unit="TFLOP/s",
+                         frac=kr["attention"]["tflops"] / groof["peak"])
+            others[gw.name] = {"tflops": r["flops"]["total"] * len(r["per"]["step"])
+                               / (r["total_ms"] * 1e-3) / 1e12,
+                               "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
+                               "kernels": kr, "roofline": groof}
+            del r
         # few query rows against many keys: the attention step splits the keys
         # over thread blocks and merges the summaries
         for lw in workloads.LONG_KEYS:

@@ -1,7 +1,8 @@
-// simt_kernels.cu - CUDA-core (FMA) kernels for the fp32 path: a tiled GEMM
-// with the head-split / plain epilogue, and masked attention folded block by
-// block with the stable summary (m, l, z) and its merge ("Stable summary of
-// an attention key block", Definition, alphabetamath.cc).
+// simt_kernels.cu - CUDA-core (FMA) kernels for the fp32 path (and bf16 heads
+// off the tensor cores): a tiled GEMM with the head-split / plain epilogue,
+// and masked attention folded block by block with the stable summary
+// (m, l, z) and its merge ("Stable summary of an attention key block",
+// Definition, alphabetamath.cc), both register-tiled.
 //
 // fp32 inputs keep 1e-4 relative accuracy here, which tf32 tensor cores
 // (10-bit mantissa) cannot; these kernels are the fp32 compute path.
@@ -100,8 +101,25 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
   }
 }
 
-constexpr int AT_ROWS = 32;  // query rows per CTA (4 per warp)
-constexpr int AT_KEYS = 32;  // keys per block (one per lane)
+constexpr int TA_C = 64;  // keys per block
+
+// 16 bytes from p as floats (zeros when !ok; p is 16-byte aligned when ok).
+__device__ __forceinline__ void load_vec(const float* p, bool ok, float (&v)[4]) {
+  const float4 a = ok ? *reinterpret_cast<const float4*>(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+  v[0] = a.x;
+  v[1] = a.y;
+  v[2] = a.z;
+  v[3] = a.w;
+}
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, bool ok, float (&v)[8]) {
+  const uint4 a = ok ? *reinterpret_cast<const uint4*>(p) : make_uint4(0, 0, 0, 0);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
 
 struct AttnParams {
   const void* Q;
@@ -111,36 +129,34 @@ struct AttnParams {
   int n_q, n_k, h, d_h, d_vh;
   float c;
   int causal, padding, pad_queries;
+  int vec_kv;  // K and V rows start on 16 bytes and hold whole 16-byte vectors
   int valid_len[MHA_MAX_PADDED_BATCH];
   int has_gate;                          // head_gate holds h entries (h <= MHA_MAX_GATED_HEADS)
   float head_gate[MHA_MAX_GATED_HEADS];  // per-head output scale, read only when has_gate
 };
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// grid (ceil(n_q / 32), h, B), 256 threads. Lane j of a warp scores key j of
-// the current 32-key block for one query row; the block's summary
-// (m_blk, l_blk, z_blk) is merged into the row's running summary. Head sizes
-// up to AT_DMAX (d_vh columns: lane + 32 t).
-template <typename T, int AT_DMAX>
+// grid (ceil(n_q / (16 RT)), h, B), 256 threads as 16 x 16 (ty, tx). A CTA
+// folds the allowed keys of 16 RT query rows, 64 keys at a time, into each
+// row's running summary (m, l, z), in base 2 (scores pre-multiplied by
+// c log2(e)). Thread (ty, tx) holds the scores of rows RT ty + i and keys
+// 4 tx + j (i < RT, j < 4), its share of each row's sum l, and z of rows
+// RT ty + i, columns tx + 16 j (j < NV; d_vh <= 16 NV). The row maximum of a
+// block is taken across the 16 threads of a row (shuffles within a half
+// warp); P goes through shared memory for z += P V. Register tiles keep a
+// dozen or more FMAs per shared-memory load.
+template <typename T, int NV, int RT>
 __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_constant__ AttnParams P) {
-  extern __shared__ float sm[];
+  constexpr int DVP = 16 * NV;
+  constexpr int TA_R = 16 * RT;  // query rows per CTA
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
   const int dq = P.d_h, dv = P.d_vh;
-  float* Qs = sm;                       // [AT_ROWS][dq]
-  float* Ks = Qs + AT_ROWS * dq;        // [AT_KEYS][dq + 1]
-  float* Vs = Ks + AT_KEYS * (dq + 1);  // [AT_KEYS][dv]
-  const int b = blockIdx.z, head = blockIdx.y, q0 = blockIdx.x * AT_ROWS;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float* Qs = sm;                  // [dq][TA_R], scaled by c log2(e)
+  float* Ks = Qs + dq * TA_R;      // [dq][TA_C]
+  float* Vs = Ks + dq * TA_C;      // [TA_C][DVP], columns past d_vh zero
+  float* Ps = Vs + TA_C * DVP;     // [TA_C][TA_R]
+  const int b = blockIdx.z, head = blockIdx.y, q0 = blockIdx.x * TA_R;
+  const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
   const int L = P.padding ? P.valid_len[b] : P.n_k;
   const int q_end = P.pad_queries ? min(L, P.n_q) : P.n_q;
   const long long bh = (long long)b * P.h + head;
@@ -148,80 +164,155 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_consta
   const T* Kg = static_cast<const T*>(P.K) + bh * P.n_k * dq;
   const T* Vg = static_cast<const T*>(P.V) + bh * P.n_k * dv;
   T* Zg = static_cast<T*>(P.Z);
+  const float cl2 = P.c * 1.4426950408889634f;
 
-  for (int e = threadIdx.x; e < AT_ROWS * dq; e += blockDim.x) {
-    const int r = e / dq, k = e % dq;
-    Qs[e] = (q0 + r < P.n_q) ? to_f(Qg[(long long)(q0 + r) * dq + k]) : 0.f;
+  for (int e = tid; e < TA_R * dq; e += 256) {
+    const int r = e % TA_R, k = e / TA_R;
+    Qs[e] = (q0 + r < P.n_q) ? to_f(Qg[(long long)(q0 + r) * dq + k]) * cl2 : 0.f;
   }
   // Keys this CTA can use: [0, k_end). Rows of K and V at or past L are never
   // read (loaded as zeros), so they may hold anything.
   int k_end = L;
-  if (P.causal) k_end = min(k_end, q0 + AT_ROWS);
+  if (P.causal) k_end = min(k_end, q0 + TA_R);
 
-  float m_run[4], l_run[4], z_run[4][AT_DMAX / 32];
+  float m_run[RT], l_run[RT], z[RT][NV];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < RT; ++i) {
     m_run[i] = -INFINITY;
     l_run[i] = 0.f;
 #pragma unroll
-    for (int t = 0; t < AT_DMAX / 32; ++t) z_run[i][t] = 0.f;
+    for (int j = 0; j < NV; ++j) z[i][j] = 0.f;
   }
 
-  for (int k0 = 0; k0 < k_end; k0 += AT_KEYS) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < AT_KEYS * dq; e += blockDim.x) {
-      const int j = e / dq, k = e % dq;
-      Ks[j * (dq + 1) + k] = (k0 + j < L) ? to_f(Kg[(long long)(k0 + j) * dq + k]) : 0.f;
-    }
-    for (int e = threadIdx.x; e < AT_KEYS * dv; e += blockDim.x) {
-      const int j = e / dv, k = e % dv;
-      Vs[e] = (k0 + j < L) ? to_f(Vg[(long long)(k0 + j) * dv + k]) : 0.f;
-    }
-    __syncthreads();
+  // 16-byte loads of K and V rows when every row starts on 16 bytes
+  constexpr int VEC = 16 / sizeof(T);
+  const bool vec = P.vec_kv;
+  for (int k0 = 0; k0 < k_end; k0 += TA_C) {
+    __syncthreads();  // the previous block's K, V and P are no longer read
+    if (vec) {
+      for (int e = tid; e < TA_C * (dq / VEC); e += 256) {
+        const int c = e / (dq / VEC), k = (e % (dq / VEC)) * VEC;
+        float v[VEC];
+        load_vec(Kg + (long long)(k0 + c) * dq + k, k0 + c < L, v);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = warp * 4 + i, q = q0 + r;
-      if (q >= q_end) continue;  // warp-uniform
-      const int key = k0 + lane;
-      const bool allowed = key < L && (!P.causal || key <= q);
-      float s = 0.f;
-      for (int k = 0; k < dq; ++k) s = fmaf(Qs[r * dq + k], Ks[lane * (dq + 1) + k], s);
-      s *= P.c;
-      const float m_blk = warp_max(allowed ? s : -INFINITY);
-      if (m_blk == -INFINITY) continue;  // empty block: the bottom summary
-      const float p = allowed ? expf(s - m_blk) : 0.f;
-      const float l_blk = warp_sum(p);
-      float z_blk[AT_DMAX / 32];
-#pragma unroll
-      for (int t = 0; t < AT_DMAX / 32; ++t) z_blk[t] = 0.f;
-      for (int j = 0; j < AT_KEYS; ++j) {
-        const float pj = __shfl_sync(0xffffffffu, p, j);
-#pragma unroll
-        for (int t = 0; t < AT_DMAX / 32; ++t) {
-          const int col = lane + 32 * t;
-          if (col < dv) z_blk[t] = fmaf(pj, Vs[j * dv + col], z_blk[t]);
-        }
+        for (int u = 0; u < VEC; ++u) Ks[(k + u) * TA_C + c] = v[u];
       }
-      // merge: m' = max(m_S, m_T); scale each side by e^{m - m'}
-      const float m_new = fmaxf(m_run[i], m_blk);
-      const float a = expf(m_run[i] - m_new), bsc = expf(m_blk - m_new);
-      l_run[i] = a * l_run[i] + bsc * l_blk;
+      for (int e = tid; e < TA_C * (DVP / VEC); e += 256) {
+        const int c = e / (DVP / VEC), col = (e % (DVP / VEC)) * VEC;
+        float v[VEC];
+        load_vec(Vg + (long long)(k0 + c) * dv + col, k0 + c < L && col < dv, v);
 #pragma unroll
-      for (int t = 0; t < AT_DMAX / 32; ++t) z_run[i][t] = a * z_run[i][t] + bsc * z_blk[t];
+        for (int u = 0; u < VEC; ++u) Vs[c * DVP + col + u] = v[u];
+      }
+    } else {
+      for (int e = tid; e < TA_C * dq; e += 256) {
+        const int c = e % TA_C, k = e / TA_C;
+        Ks[e] = (k0 + c < L) ? to_f(Kg[(long long)(k0 + c) * dq + k]) : 0.f;
+      }
+      for (int e = tid; e < TA_C * DVP; e += 256) {
+        const int c = e / DVP, col = e % DVP;
+        Vs[e] = (k0 + c < L && col < dv) ? to_f(Vg[(long long)(k0 + c) * dv + col]) : 0.f;
+      }
+    }
+    __syncthreads();
+    // scores of this thread's 4 x 4 tile
+    float s[RT][4];
+#pragma unroll
+    for (int i = 0; i < RT; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < dq; ++k) {
+      float qa[RT];
+#pragma unroll
+      for (int i4 = 0; i4 < RT; i4 += 4) {
+        const float4 qv = *reinterpret_cast<const float4*>(Qs + k * TA_R + RT * ty + i4);
+        qa[i4] = qv.x;
+        qa[i4 + 1] = qv.y;
+        qa[i4 + 2] = qv.z;
+        qa[i4 + 3] = qv.w;
+      }
+      const float4 kv = *reinterpret_cast<const float4*>(Ks + k * TA_C + 4 * tx);
+      const float ka[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+      for (int i = 0; i < RT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qa[i], ka[j], s[i][j]);
+    }
+    // fold the block into each row's summary
+    float pcol[RT][4];  // p of key 4 tx + j, row RT ty + i
+#pragma unroll
+    for (int i = 0; i < RT; ++i) {
+      const int q = q0 + RT * ty + i;
+      float mb = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int key = k0 + 4 * tx + j;
+        const bool allowed = key < L && (!P.causal || key <= q);
+        if (!allowed) s[i][j] = -INFINITY;  // weight exactly 0
+        mb = fmaxf(mb, s[i][j]);
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+      const float m_new = fmaxf(m_run[i], mb);
+      // e^{m - m'} (1 when m is kept, also while the row has no allowed key yet)
+      const float a = (m_new == m_run[i]) ? 1.f : ex2_approx(m_run[i] - m_new);
+      float ls = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float p = (s[i][j] == -INFINITY) ? 0.f : ex2_approx(s[i][j] - m_new);
+        pcol[i][j] = p;
+        ls += p;
+      }
+      l_run[i] = l_run[i] * a + ls;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) z[i][j] *= a;
       m_run[i] = m_new;
     }
-  }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int q = q0 + warp * 4 + i;
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i4 = 0; i4 < RT; i4 += 4)
+        *reinterpret_cast<float4*>(Ps + (4 * tx + j) * TA_R + RT * ty + i4) =
+            make_float4(pcol[i4][j], pcol[i4 + 1][j], pcol[i4 + 2][j], pcol[i4 + 3][j]);
+    __syncthreads();
+    // z += P V over the block's keys
+    const int nc = min(TA_C, k_end - k0);
+#pragma unroll 4
+    for (int c = 0; c < nc; ++c) {
+      float pa[RT];
+#pragma unroll
+      for (int i4 = 0; i4 < RT; i4 += 4) {
+        const float4 pv = *reinterpret_cast<const float4*>(Ps + c * TA_R + RT * ty + i4);
+        pa[i4] = pv.x;
+        pa[i4 + 1] = pv.y;
+        pa[i4 + 2] = pv.z;
+        pa[i4 + 3] = pv.w;
+      }
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const float v = Vs[c * DVP + tx + 16 * j];
+#pragma unroll
+        for (int i = 0; i < RT; ++i) z[i][j] = fmaf(pa[i], v, z[i][j]);
+      }
+    }
+  }
+  // the row sum is spread over the row's 16 threads
+#pragma unroll
+  for (int i = 0; i < RT; ++i)
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], o);
+#pragma unroll
+  for (int i = 0; i < RT; ++i) {
+    const int q = q0 + RT * ty + i;
     if (q >= P.n_q) continue;
     const bool computed = q < q_end;
     const float inv = computed ? (P.has_gate ? P.head_gate[head] : 1.f) / l_run[i] : 0.f;
     T* zrow = Zg + ((long long)b * P.n_q + q) * (long long)P.h * dv + (long long)head * dv;
 #pragma unroll
-    for (int t = 0; t < AT_DMAX / 32; ++t) {
-      const int col = lane + 32 * t;
-      if (col < dv) zrow[col] = from_f<T>(computed ? z_run[i][t] * inv : 0.f);
+    for (int j = 0; j < NV; ++j) {
+      const int col = tx + 16 * j;
+      if (col < dv) zrow[col] = from_f<T>(computed ? z[i][j] * inv : 0.f);
     }
   }
 }
@@ -248,15 +339,33 @@ mha_status gemm_simt(const GemmProblem* probs, int nprob, mha_dtype dt, cudaStre
 
 namespace {
 
-template <typename T, int DMAX>
-mha_status launch_attention_simt(const AttnParams& P, const dim3& grid, size_t smem,
-                                 cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(attention_simt_kernel<T, DMAX>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return MHA_ERR_CUDA;
-  attention_simt_kernel<T, DMAX><<<grid, 256, smem, s>>>(P);
+template <typename T, int NV, int RT>
+mha_status launch_attention_simt(const AttnParams& P, int B, cudaStream_t s) {
+  constexpr int TA_R = 16 * RT;
+  const dim3 grid((P.n_q + TA_R - 1) / TA_R, P.h, B);
+  if (grid.y > 65535u || grid.z > 65535u) return MHA_ERR_UNSUPPORTED;
+  const size_t smem =
+      sizeof(float) * ((size_t)P.d_h * (TA_R + TA_C) + (size_t)TA_C * 16 * NV + TA_C * TA_R);
+  if (!ensure_smem_limit((const void*)attention_simt_kernel<T, NV, RT>, (int)smem))
+    return MHA_ERR_CUDA;
+  attention_simt_kernel<T, NV, RT><<<grid, 256, smem, s>>>(P);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+// Narrow value heads take 8 query rows per thread (more FMAs per shared
+// load) when that still leaves two CTAs per SM, wide ones 4 (registers for z).
+template <typename T>
+mha_status launch_attention_simt_dv(const AttnParams& P, int B, cudaStream_t s) {
+  const bool tall = (long long)((P.n_q + 127) / 128) * P.h * B >= 2LL * num_sms();
+  if (P.d_vh <= 16)
+    return tall ? launch_attention_simt<T, 1, 8>(P, B, s) : launch_attention_simt<T, 1, 4>(P, B, s);
+  if (P.d_vh <= 32)
+    return tall ? launch_attention_simt<T, 2, 8>(P, B, s) : launch_attention_simt<T, 2, 4>(P, B, s);
+  if (P.d_vh <= 64)
+    return tall ? launch_attention_simt<T, 4, 8>(P, B, s) : launch_attention_simt<T, 4, 4>(P, B, s);
+  if (P.d_vh <= 128) return launch_attention_simt<T, 8, 4>(P, B, s);
+  return launch_attention_simt<T, 16, 4>(P, B, s);
 }
 
 }  // namespace
@@ -277,21 +386,18 @@ mha_status attention_simt(const AttnArgs& a, mha_dtype dt, cudaStream_t s) {
   P.causal = a.causal;
   P.padding = a.padding;
   P.pad_queries = a.pad_queries;
+  {
+    const int vec = dt == MHA_DTYPE_F32 ? 4 : 8;  // elements per 16 bytes
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    P.vec_kv = a.d_h % vec == 0 && a.d_vh % vec == 0 && al16(a.K) && al16(a.V);
+  }
   for (int b = 0; b < MHA_MAX_PADDED_BATCH; ++b)
     P.valid_len[b] = (a.padding && b < a.B) ? a.valid_len_host[b] : a.n_k;
   P.has_gate = a.head_gate_host != nullptr && a.h <= MHA_MAX_GATED_HEADS;
   for (int i = 0; i < MHA_MAX_GATED_HEADS; ++i)
     P.head_gate[i] = (P.has_gate && i < a.h) ? a.head_gate_host[i] : 1.f;
-  const size_t smem =
-      sizeof(float) * (AT_ROWS * a.d_h + AT_KEYS * (a.d_h + 1) + AT_KEYS * a.d_vh);
-  const dim3 grid((a.n_q + AT_ROWS - 1) / AT_ROWS, a.h, a.B);
-  if (grid.y > 65535u || grid.z > 65535u) return MHA_ERR_UNSUPPORTED;
-  const bool wide = a.d_vh > 128;
-  if (dt == MHA_DTYPE_F32)
-    return wide ? launch_attention_simt<float, 256>(P, grid, smem, s)
-                : launch_attention_simt<float, 128>(P, grid, smem, s);
-  return wide ? launch_attention_simt<__nv_bfloat16, 256>(P, grid, smem, s)
-              : launch_attention_simt<__nv_bfloat16, 128>(P, grid, smem, s);
+  if (dt == MHA_DTYPE_F32) return launch_attention_simt_dv<float>(P, a.B, s);
+  return launch_attention_simt_dv<__nv_bfloat16>(P, a.B, s);
 }
 
 }  // namespace mha

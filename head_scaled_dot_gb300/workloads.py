@@ -70,6 +70,13 @@ GENERAL_DIMS = _w("self_bf16_B4_T1024_d768_h8_dh96_none", 4, 1024, 768, 8, 96, "
                   1 / math.sqrt(96), 6)
 
 
+# A head size off the tensor cores (d_h = 32): the attention step runs in the
+# CUDA-core kernel. Measured beside the others against the fp32 FMA peak;
+# seed 9.
+SIMT_DIMS = _w("self_bf16_B4_T1024_d768_h24_dh32_none", 4, 1024, 768, 24, 32, "none", "bf16",
+               1 / math.sqrt(32), 9)
+
+
 # Few query rows against many keys (the cross-attention workload's heads with
 # n_q of 64 or 128 and n_k = 32768, 16 (batch item, head) pairs): 16 query
 # tile pairs would fill 16 of the SMs, so the attention step splits the keys
