@@ -4,7 +4,8 @@
 //        review", "Separate and Combined Projections");
 //   out: Y = Z W_O ("The Complete Multi-Head Operation").
 //
-// Persistent kernel, one CTA per SM, 128 x BN output tiles (BN = 256 or 128),
+// Persistent kernel, one CTA per SM (or clusters of two, see gemm_tc_kernel),
+// 128 x BN output tiles (BN = 256 or 128),
 // 64-deep K blocks in a STAGES-deep shared-memory ring filled by TMA. The
 // problems that share their A operand (the QKV projections of one input) form
 // a group whose tiles run M panel by M panel, each 128-row panel of A through
@@ -20,6 +21,8 @@
 // (row-major X), B is MN-major (row-major W): both straight from the caller's
 // layout, no transpose or packing pass.
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -43,6 +46,7 @@ struct GemmTcHead {
   int g_first[MAXP + 1];   // problems [g_first[g], g_first[g + 1]) form group g
   int g_ntiles[MAXP];      // N tiles of one M panel through all of group g
   int g_select[MAXP];      // group g multiplies only the selected panels
+  int g_panels[MAXP];      // M panels of group g (selected ones only, for g_select)
   int g_start[MAXP + 1];   // first tile of group g; g_start[ngroups]: product tiles
   int zero_prob;           // problem whose unselected panels are written as zeros
   int zero_tiles;          // tiles [g_start[ngroups], + zero_tiles): zero fills
@@ -90,19 +94,14 @@ struct Tile {
   bool zero;  // write zeros, no product
 };
 
+// Product tile t of a cluster of CL CTAs, for the CTA of rank `rank`: the
+// cluster's tiles have the same N tile and CL consecutive M panels of one
+// group (a panel past the group's last is a tile of rows past M: its A loads
+// are zero fill and its rows are not stored).
 template <class Params>
-__device__ __forceinline__ Tile decode_tile(const Params& P, int t, int bn) {
+__device__ __forceinline__ Tile decode_tile(const Params& P, int t, int bn, int CL, int rank) {
   const GemmTcHead& H = P.h;
   Tile r;
-  const int prod = H.g_start[H.ngroups];
-  if (t >= prod) {
-    const int z = t - prod, tn = H.tiles_n[H.zero_prob];
-    r.p = H.zero_prob;
-    r.m0 = panel_of(P.zrun_m, P.zrun_pre, H.nzrun, z / tn) * BM;
-    r.n0 = (z % tn) * bn;
-    r.zero = true;
-    return r;
-  }
   int g = 0;
   while (g + 1 < H.ngroups && t >= H.g_start[g + 1]) ++g;
   const int local = t - H.g_start[g];
@@ -111,9 +110,26 @@ __device__ __forceinline__ Tile decode_tile(const Params& P, int t, int bn) {
   int p = H.g_first[g];
   while (rr >= H.tiles_n[p]) rr -= H.tiles_n[p++];
   r.p = p;
-  r.m0 = (H.g_select[g] ? panel_of(P.run_m, P.run_pre, H.nrun, k) : k) * BM;
+  const int panel = CL * k + rank;
+  if (panel >= H.g_panels[g])
+    r.m0 = (H.prob[p].M + BM - 1) / BM * BM;
+  else
+    r.m0 = (H.g_select[g] ? panel_of(P.run_m, P.run_pre, H.nrun, panel) : panel) * BM;
   r.n0 = rr * bn;
   r.zero = false;
+  return r;
+}
+
+// Zero-fill tile z (rows with nothing to multiply).
+template <class Params>
+__device__ __forceinline__ Tile decode_zero_tile(const Params& P, int z, int bn) {
+  const GemmTcHead& H = P.h;
+  Tile r;
+  const int tn = H.tiles_n[H.zero_prob];
+  r.p = H.zero_prob;
+  r.m0 = panel_of(P.zrun_m, P.zrun_pre, H.nzrun, z / tn) * BM;
+  r.n0 = (z % tn) * bn;
+  r.zero = true;
   return r;
 }
 
@@ -151,11 +167,19 @@ __device__ __forceinline__ void store_row32(const GemmProblem& pr, long long row
   }
 }
 
-template <int BN, int RUNS>
+// CL = 2: the kernel runs in clusters of two CTAs that compute vertically
+// adjacent tiles with the same N tile. Each CTA loads its own A panel and
+// half of the W tile, multicast into both CTAs' shared memory, so the W
+// tile is read from L2 once per pair; a stage is refilled only after both
+// CTAs' MMAs are done with it (their commits arrive on both CTAs' empty
+// barriers).
+template <int BN, int RUNS, int CL>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ GemmTcParams<RUNS> P) {
   using C = Cfg<BN>;
   const GemmTcHead& H = P.h;
+  const int rank = CL > 1 ? (int)cluster_rank() : 0;
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;  // cluster and clusters
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -170,7 +194,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);  // one MMA commit per CTA of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -185,6 +209,8 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // the other CTA's barriers are initialized before anything is multicast
+  if (CL > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // The prologue above touched only this CTA's shared and tensor memory. The
@@ -193,8 +219,7 @@ __global__ void __launch_bounds__(192, 1)
   grid_dep_launch_dependents();
   grid_dep_wait();
   const WaitCtl w{H.err, abort_flag, H.limit_ns};
-  const int prod = H.g_start[H.ngroups];       // tiles with a product
-  const int total = prod + H.zero_tiles;       // and the zero fills after them
+  const int prod = H.g_start[H.ngroups];       // product tiles (per cluster)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -205,8 +230,8 @@ __global__ void __launch_bounds__(192, 1)
       }
       uint32_t it = 0;  // global k-block counter across tiles
       bool ok = true;
-      for (int t = blockIdx.x; t < prod && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(P, t, BN);
+      for (int t = cid; t < prod && ok; t += ncl) {
+        const Tile tl = decode_tile(P, t, BN, CL, rank);
         const int kblocks = (H.prob[tl.p].K + BK - 1) / BK;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % C::STAGES;
@@ -218,14 +243,29 @@ __global__ void __launch_bounds__(192, 1)
           uint8_t* b_s = a_s + C::A_BYTES;
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
           tma_load_2d(a_s, &H.amap[tl.p], &full[s], kb * BK, tl.m0);
+          if (CL == 1) {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(b_s + j * (BK * 128), &H.bmap[tl.p], &full[s], tl.n0 + 64 * j, kb * BK);
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_s + j * (BK * 128), &H.bmap[tl.p], &full[s], tl.n0 + 64 * j, kb * BK);
+          } else {
+            // this CTA's share of the W tile, into both CTAs
+            constexpr int PER = BN / 64 / CL;
+#pragma unroll
+            for (int j = rank * PER; j < (rank + 1) * PER; ++j)
+              tma_load_2d_mc(b_s + j * (BK * 128), &H.bmap[tl.p], &full[s], tl.n0 + 64 * j,
+                             kb * BK, (uint16_t)((1u << CL) - 1));
+          }
         }
       }
       if (!ok) {  // let the loads this CTA started land before it exits
         for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
           drain_wait(&full[k % C::STAGES], (k / C::STAGES) & 1);
+      }
+      if (CL > 1) {
+        // the other CTA's last commits arrive on this CTA's empty barriers:
+        // they must have landed before this CTA's shared memory is released
+        for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
+          drain_wait(&empty[k % C::STAGES], (k / C::STAGES) & 1);
       }
     }
   } else if (warp == 1) {
@@ -233,8 +273,8 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 1);
       uint32_t it = 0, tile_i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < prod && ok; t += gridDim.x, ++tile_i) {
-        const Tile tl = decode_tile(P, t, BN);
+      for (int t = cid; t < prod && ok; t += ncl, ++tile_i) {
+        const Tile tl = decode_tile(P, t, BN, CL, rank);
         const int kblocks = (H.prob[tl.p].K + BK - 1) / BK;
         const uint32_t buf = tile_i & 1;
         // wait until the epilogue has drained this accumulator buffer
@@ -261,7 +301,12 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t bd = sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024);
             umma_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0);
           }
-          umma_commit(&empty[s]);  // frees the stage once these MMAs finish
+          // frees the stage once these MMAs finish (in every CTA of the cluster,
+          // whose W halves it holds)
+          if (CL == 1)
+            umma_commit(&empty[s]);
+          else
+            umma_commit_mc(&empty[s], (uint16_t)((1u << CL) - 1));
         }
         if (ok) umma_commit(&acc_full[buf]);
       }
@@ -273,12 +318,21 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // Epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4) .. +31.
+    // Epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4) .. +31. The
+    // cluster's product tiles, then (one CTA at a time) the zero fills.
     const int g = warp & 3;
     uint32_t tile_i = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile(P, t, BN);
+    const int nprod = (prod - cid + ncl - 1) / ncl;  // product tiles of this CTA
+    for (int i = 0;; ++i) {
+      Tile tl;
+      if (i < nprod) {
+        tl = decode_tile(P, cid + i * ncl, BN, CL, rank);
+      } else {
+        const int z = blockIdx.x + (i - nprod) * (int)gridDim.x;
+        if (z >= H.zero_tiles) break;
+        tl = decode_zero_tile(P, z, BN);
+      }
       const GemmProblem& pr = H.prob[tl.p];
       const int m = tl.m0 + 32 * g + lane;
       const bool row_ok = m < pr.M;
@@ -326,23 +380,73 @@ __global__ void __launch_bounds__(192, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a cluster leaves while the other may still write into it
+  if (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-template <int BN, int RUNS>
-mha_status launch_kernel(const GemmTcParams<RUNS>& P, int grid, cudaStream_t s) {
+// Clusters of CL CTAs of this kernel that can be resident at once on the
+// current device (a cluster's CTAs share a GPC), asked once per device.
+template <int BN, int RUNS, int CL>
+int max_clusters() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms() / CL;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL * (num_sms() / CL));
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, RUNS, CL>, &cfg) != cudaSuccess ||
+        n < 1)
+      n = num_sms() / CL;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int BN, int RUNS, int CL>
+mha_status launch_kernel(const GemmTcParams<RUNS>& P, int clusters, cudaStream_t s) {
   using C = Cfg<BN>;
-  if (!ensure_smem_limit((const void*)gemm_tc_kernel<BN, RUNS>, C::SMEM)) return MHA_ERR_CUDA;
-  const cudaError_t e =
-      launch_dependent(gemm_tc_kernel<BN, RUNS>, dim3(grid), dim3(192), C::SMEM, s, P);
+  auto kernel = gemm_tc_kernel<BN, RUNS, CL>;
+  if (!ensure_smem_limit((const void*)kernel, C::SMEM)) return MHA_ERR_CUDA;
+  const int cap = max_clusters<BN, RUNS, CL>();
+  if (clusters > cap) clusters = cap;
+  const int grid = clusters * CL;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, P);
   count_launch();
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
-template <int BN>
+// Tiles per cluster of CL CTAs: a group's M panels are taken CL at a time.
+template <int BN, int CL>
 mha_status launch(GemmTcParams<MAXRUNS>& P, int nprob, int sel_panels, int unsel_panels,
                   cudaStream_t s) {
   GemmTcHead& H = P.h;
@@ -354,15 +458,21 @@ mha_status launch(GemmTcParams<MAXRUNS>& P, int nprob, int sel_panels, int unsel
     H.g_ntiles[g] = nt;
     const GemmProblem& pr = H.prob[H.g_first[g]];
     const long long panels = H.g_select[g] ? sel_panels : (pr.M + BM - 1) / BM;
+    if (panels > (1ll << 30)) return MHA_ERR_UNSUPPORTED;
+    H.g_panels[g] = (int)panels;
     H.g_start[g] = start;
-    const long long tiles = (long long)start + panels * nt;
+    const long long tiles = (long long)start + (panels + CL - 1) / CL * nt;
     if (tiles > (1ll << 30)) return MHA_ERR_UNSUPPORTED;
     start = (int)tiles;
   }
   H.g_start[H.ngroups] = start;
   H.zero_tiles = H.zero_prob >= 0 ? unsel_panels * H.tiles_n[H.zero_prob] : 0;
-  const int total = start + H.zero_tiles;
-  const int grid = total < num_sms() ? total : num_sms();
+  // clusters for the product tiles, and CTAs enough for the zero fills
+  int clusters = start;
+  const int zero_cl = (H.zero_tiles + CL - 1) / CL;
+  if (zero_cl > clusters) clusters = zero_cl;
+  if (clusters > num_sms() / CL) clusters = num_sms() / CL;
+  if (clusters < 1) clusters = 1;
   if (H.nrun <= SMALL_RUNS && H.nzrun <= SMALL_RUNS) {
     GemmTcParams<SMALL_RUNS> Q;
     Q.h = H;
@@ -372,9 +482,9 @@ mha_status launch(GemmTcParams<MAXRUNS>& P, int nprob, int sel_panels, int unsel
       Q.zrun_m[r] = P.zrun_m[r];
       Q.zrun_pre[r] = P.zrun_pre[r];
     }
-    return launch_kernel<BN, SMALL_RUNS>(Q, grid, s);
+    return launch_kernel<BN, SMALL_RUNS, CL>(Q, clusters, s);
   }
-  return launch_kernel<BN, MAXRUNS>(P, grid, s);
+  return launch_kernel<BN, MAXRUNS, CL>(P, clusters, s);
 }
 
 // Runs of selected and of unselected 128-row panels of the B * rows_per_batch
@@ -487,8 +597,24 @@ mha_status gemm_tc(const GemmProblem* probs, int nprob, const RowSelect* sel, in
       H.zero_prob = 0;
     }
   }
-  return all256 ? launch<256>(P, nprob, sel_panels, unsel_panels, s)
-                : launch<128>(P, nprob, sel_panels, unsel_panels, s);
+  // Pairs of CTAs share the W tile (multicast) for the grouped projections
+  // with many tiles (measured on GB300: 4-11 % faster there; no gain for a
+  // single problem or a few hundred tiles, where the pair's lockstep costs
+  // what the halved W reads save).
+  const int bn = all256 ? 256 : 128;
+  long long tiles = 0;
+  for (int g = 0; g < H.ngroups; ++g) {
+    long long nt = 0;
+    for (int p = H.g_first[g]; p < H.g_first[g + 1]; ++p) nt += (probs[p].N + bn - 1) / bn;
+    const GemmProblem& pr = probs[H.g_first[g]];
+    tiles += (H.g_select[g] ? sel_panels : (pr.M + BM - 1) / BM) * nt;
+  }
+  const bool pair = nprob > 1 && tiles >= 4LL * num_sms();
+  if (!pair)
+    return all256 ? launch<256, 1>(P, nprob, sel_panels, unsel_panels, s)
+                  : launch<128, 1>(P, nprob, sel_panels, unsel_panels, s);
+  return all256 ? launch<256, 2>(P, nprob, sel_panels, unsel_panels, s)
+                : launch<128, 2>(P, nprob, sel_panels, unsel_panels, s);
 }
 
 }  // namespace mha

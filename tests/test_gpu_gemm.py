@@ -150,3 +150,36 @@ def test_general_form_three_inputs_three_groups():
     ref = oracle.mha_forward_general(f64(X_q), f64(X_k), f64(X_v), f64(W_Q), f64(W_K), f64(W_V),
                                      f64(W_O), h, d, d, 0.125, oracle.MASK_PADDING, lens, False)
     assert rel_err(f64(Y), ref) <= 1e-2
+
+
+@pytest.mark.parametrize("B,T,lens,cross", [
+    (5, 1408, None, False),               # 55 panels (odd): one pair's second tile has no rows
+    (5, 1408, [1408, 300, 1217, 1408, 1000], False),  # 43 selected panels (odd)
+    (3, 512, None, True),                 # cross: K and V over 1536 rows of X_kv per item
+])
+def test_qkv_projection_in_cta_pairs_exact_on_integers(B, T, lens, cross):
+    """Grouped projections with more tiles than four per SM run in pairs of
+    CTAs that share the W tile (multicast). Small integers are exact in bf16
+    and in the fp32 accumulator, so Q, K and V must match bit for bit, also
+    for a pair whose second panel is past the last one and with only the
+    selected panels of a padding mask computed."""
+    g = torch.Generator().manual_seed(B * T + (lens is not None) + 2 * cross)
+    d_model, h, d_h, d_vh = 256, 16, 128, 128  # 24 N tiles of 256 per M panel: > 608 tiles
+    n_k = 3 * T if cross else T
+    X = torch.randint(-2, 3, (B, T, d_model), generator=g).bfloat16()
+    Xkv = torch.randint(-2, 3, (B, n_k, d_model), generator=g).bfloat16() if cross else None
+    WQ = torch.randint(-2, 3, (d_model, h * d_h), generator=g).bfloat16()
+    WK = torch.randint(-2, 3, (d_model, h * d_h), generator=g).bfloat16()
+    WV = torch.randint(-2, 3, (d_model, h * d_vh), generator=g).bfloat16()
+    mask = "padding" if lens is not None else "none"
+    Q, K, V = mha.qkv_projection(X.cuda(), None if Xkv is None else Xkv.cuda(), WQ.cuda(),
+                                 WK.cuda(), WV.cuda(), h, d_h, d_vh, mask=mask, valid_len=lens)
+    torch.cuda.synchronize()
+    src_kv = Xkv if cross else X
+    for name, got, src, Wt, d, n in (("Q", Q, X, WQ, d_h, T), ("K", K, src_kv, WK, d_h, n_k),
+                                     ("V", V, src_kv, WV, d_vh, n_k)):
+        ref = (f64(src) @ f64(Wt)).reshape(B, n, h, d).transpose(0, 2, 1, 3)
+        got = f64(got)
+        for b in range(B):
+            rows = n if lens is None else min(n, -(-lens[b] // 128) * 128)
+            assert np.array_equal(got[b, :, :rows], ref[b, :, :rows]), (name, b)
