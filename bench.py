@@ -1,6 +1,7 @@
 """Benchmark of the multi-head attention forward pass on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I | --workload NAME]
+                    [--impl ours|reference]
 
 One step is one whole forward pass (the QKV projection with head split, the
 fused attention kernel and the output projection) over one batch of seeded
@@ -66,6 +67,10 @@ def parse():
                     help="workload index (0..4); the JSON line is for this one (default: 3, "
                          "the largest: B=2, T=8192, d_model=2048, h=16, d_h=128, causal + "
                          "padding)")
+    ap.add_argument("--workload", default=None,
+                    help="time this named workload instead of --config (any name of "
+                         "head_scaled_dot_gb300.workloads: the five, the general head sizes, "
+                         "the long-key ones)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-others", action="store_true",
                     help="skip the per-workload table of the other bf16 workloads")
@@ -75,6 +80,20 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true",
                     help="skip the clock-sampling window (for profiler runs)")
     return ap.parse_args()
+
+
+def chosen_workload(args):
+    """The workload of the JSON line: --workload by name, else --config."""
+    from head_scaled_dot_gb300 import workloads
+    if args.workload:
+        named = {w.name: w for w in workloads.WORKLOADS + [workloads.GENERAL_DIMS,
+                                                           workloads.SIMT_DIMS]
+                 + workloads.LONG_KEYS}
+        if args.workload not in named:
+            raise SystemExit("unknown workload %r; one of: %s" % (args.workload,
+                                                                 ", ".join(sorted(named))))
+        return named[args.workload]
+    return workloads.WORKLOADS[args.config]
 
 
 def peaks():
@@ -487,7 +506,7 @@ def run_reference(args):
     if rank != 0:
         return
     from head_scaled_dot_gb300 import workloads
-    w = workloads.WORKLOADS[args.config]
+    w = chosen_workload(args)
     inp = workloads.make_inputs(w)
     lens = None if inp["valid_len"] is None else [int(x) for x in inp["valid_len"]]
     units = [(b, i) for b in range(w.B) for i in range(w.h)]
@@ -540,10 +559,23 @@ def roofline(w, krows, pk, pk_kind, dev):
     roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "peak_kind": pk_kind + " burst",
             "ms_per_launch": krows[dom]["ms"], "traffic": stored_traffic(dom, w.name)}
-    if w.dtype == "f32":  # every kernel of the fp32 path runs on the CUDA cores
+    attn_cuda_cores = w.dtype == "f32" or not all(64 <= d <= 128 and d % 8 == 0
+                                                  for d in (w.d_h, w.d_vh))
+    if w.dtype == "f32" or (dom == "attention" and attn_cuda_cores):
+        # the fp32 path, and attention of head sizes off the tensor cores, run
+        # on the CUDA cores
         alu = alu_peak_tflops(dev, sm_max_mhz())
         roof.update(bound="alu", peak=alu, frac=ach / alu,
                     peak_kind="derived: SMs x 128 FP32 lanes x 2 flop x max SM clock")
+    elif dom == "attention" and w.n_q <= 128:
+        # few query rows: 4 n_q d_h flop per key against 2 (d_h + d_vh) bytes of
+        # K and V is below the ridge, so the bound is reading Q, K, V and
+        # writing Z once
+        nbytes = w.B * w.h * (w.n_q + w.n_k) * (w.d_h + w.d_vh) * 2
+        gbs = nbytes / (krows[dom]["ms"] * 1e-3) / 1e9
+        roof.update(bound="hbm", achieved=gbs, peak=pk["hbm_gbs"], unit="GB/s",
+                    frac=gbs / pk["hbm_gbs"], peak_kind=pk_kind + " copy bandwidth",
+                    bytes_per_launch=nbytes, attention_tflops=ach)
     return roof
 
 
@@ -555,7 +587,7 @@ def run_ours(args):
     from head_scaled_dot_gb300 import mha, workloads
     mha.load()
     pk, pk_kind = peaks()
-    w = workloads.WORKLOADS[args.config]
+    w = chosen_workload(args)
     res = measure_workload(w, args.steps, args.warmup, dev, world, e2e=not args.no_e2e,
                            sample_clocks=not args.no_clocks)
     total_ms = max_over_ranks(res["total_ms"], world, dev)
@@ -566,7 +598,7 @@ def run_ours(args):
     others = {}
     if not args.no_others and rank == 0:
         for j, wj in enumerate(workloads.WORKLOADS):
-            if j == args.config or wj.dtype != "bf16":
+            if wj.name == w.name or wj.dtype != "bf16":
                 continue
             r = measure_workload(wj, max(3, args.steps // 2), 3, dev, 1, e2e=False,
                                  sample_clocks=False)
