@@ -72,7 +72,10 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
   static constexpr int B_BYTES = BK * BN * 2;   // 32 KB (BN = 256)
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // epilogue staging: per epilogue warp 32 rows x 64 columns of bf16
+  static constexpr int STAGING_BYTES = 4 * 32 * 128;
+  static constexpr int SMEM =
+      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // double-buffered accumulator
 };
 
@@ -143,26 +146,37 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Stores one thread's 32 output columns [n, n + 32) of row m (packed bf16
-// pairs) through the problem's index map.
-__device__ __forceinline__ void store_row32(const GemmProblem& pr, long long row_off, int n,
-                                            const uint32_t (&pk)[16]) {
+// Output offset of row m's element (m, n) through the problem's index map,
+// split into the row part (row_offset) and the column part.
+__device__ __forceinline__ long long row_offset(const GemmProblem& pr, int m) {
+  return (long long)(m / pr.rows_per_group) * pr.s_group_row +
+         (long long)(m % pr.rows_per_group) * pr.s_row;
+}
+
+// Writes a warp's 32 rows x 64 columns [n, n + 64) of a tile (rows m0w ..
+// m0w + 31) to the output: the rows sit in the warp's shared-memory staging
+// area `st` (row r: 8 chunks of 8 bf16, chunk k at position k ^ (r & 7)),
+// and each store instruction writes 4 rows x 128 contiguous bytes. `rowoff`
+// is lane r's row_offset of row m0w + r (valid when that row is below M);
+// `zero`: write zeros instead of the staged values. Every 8-column chunk
+// lies inside one column group (N and cols_per_group are multiples of 8), so
+// it is stored whole or, past N, not at all.
+__device__ __forceinline__ void store_warp_rows(const GemmProblem& pr, const uint4* st, int m0w,
+                                                long long rowoff, int n, bool zero, int lane) {
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(pr.out);
-  const long long off =
-      row_off + (long long)(n / pr.cols_per_group) * pr.s_group_col + (n % pr.cols_per_group);
-  if (n + 32 <= pr.N && (n % pr.cols_per_group) + 32 <= pr.cols_per_group) {
-    uint4* dst = reinterpret_cast<uint4*>(out + off);
+  // a lane always stores chunk cc = lane % 8 of rows 4 it + lane / 8
+  const int cc = lane & 7;
+  const int nn = n + 8 * cc;
+  const long long coloff =
+      (long long)(nn / pr.cols_per_group) * pr.s_group_col + (nn % pr.cols_per_group);
+  const bool col_ok = nn < pr.N;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-  } else {
-    for (int j = 0; j < 32 && n + j < pr.N; ++j) {
-      const int nn = n + j;
-      const long long o = row_off + (long long)(nn / pr.cols_per_group) * pr.s_group_col +
-                          (nn % pr.cols_per_group);
-      const uint32_t word = pk[j >> 1];
-      const uint16_t bits = (j & 1) ? (uint16_t)(word >> 16) : (uint16_t)(word & 0xFFFF);
-      out[o] = __ushort_as_bfloat16(bits);
+  for (int it = 0; it < 8; ++it) {
+    const int r = 4 * it + (lane >> 3);
+    const long long ro = __shfl_sync(0xffffffffu, rowoff, r);
+    if (col_ok && m0w + r < pr.M) {
+      const uint4 v = zero ? make_uint4(0, 0, 0, 0) : st[r * 8 + (cc ^ (r & 7))];
+      *reinterpret_cast<uint4*>(out + ro + coloff) = v;
     }
   }
 }
@@ -183,7 +197,8 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint4* staging = reinterpret_cast<uint4*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;   // [2]
   uint64_t* acc_empty = acc_full + 2;       // [2]
@@ -203,6 +218,19 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // The producer thread fetches the descriptors and decodes its first tile
+  // (parameters only) before the grid dependency wait, so that its first
+  // loads go out as soon as the previous kernel's results may be read.
+  const int prod = H.g_start[H.ngroups];  // product tiles (per cluster)
+  Tile first{};
+  if (threadIdx.x == 0) {
+    for (int p = 0; p < MAXP; ++p) {
+      if (p >= H.g_first[H.ngroups]) break;
+      tma_prefetch_desc(&H.amap[p]);
+      tma_prefetch_desc(&H.bmap[p]);
+    }
+    if (cid < prod) first = decode_tile(P, cid, BN, CL, rank);
+  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
@@ -219,19 +247,13 @@ __global__ void __launch_bounds__(192, 1)
   grid_dep_launch_dependents();
   grid_dep_wait();
   const WaitCtl w{H.err, abort_flag, H.limit_ns};
-  const int prod = H.g_start[H.ngroups];       // product tiles (per cluster)
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int p = 0; p < MAXP; ++p) {
-        if (p >= H.g_first[H.ngroups]) break;
-        tma_prefetch_desc(&H.amap[p]);
-        tma_prefetch_desc(&H.bmap[p]);
-      }
       uint32_t it = 0;  // global k-block counter across tiles
       bool ok = true;
       for (int t = cid; t < prod && ok; t += ncl) {
-        const Tile tl = decode_tile(P, t, BN, CL, rank);
+        const Tile tl = t == cid ? first : decode_tile(P, t, BN, CL, rank);
         const int kblocks = (H.prob[tl.p].K + BK - 1) / BK;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % C::STAGES;
@@ -318,57 +340,56 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // Epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4) .. +31. The
-    // cluster's product tiles, then (one CTA at a time) the zero fills.
+    // Epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4) .. +31. First
+    // this CTA's zero fills (one CTA at a time over the zero tiles), while
+    // the first product tile is still being multiplied; then the cluster's
+    // product tiles. Rows go out through the warp's staging area, 4 rows of
+    // 128 contiguous bytes per store instruction.
     const int g = warp & 3;
+    uint4* st = staging + g * (32 * 8);
+    for (int z = blockIdx.x; z < H.zero_tiles; z += (int)gridDim.x) {
+      const Tile tl = decode_zero_tile(P, z, BN);
+      const GemmProblem& pr = H.prob[tl.p];
+      const int m0w = tl.m0 + 32 * g;
+      const long long ro = m0w + lane < pr.M ? row_offset(pr, m0w + lane) : 0;
+      for (int c = 0; c < BN; c += 64) store_warp_rows(pr, st, m0w, ro, tl.n0 + c, true, lane);
+    }
     uint32_t tile_i = 0;
     bool ok = true;
     const int nprod = (prod - cid + ncl - 1) / ncl;  // product tiles of this CTA
-    for (int i = 0;; ++i) {
-      Tile tl;
-      if (i < nprod) {
-        tl = decode_tile(P, cid + i * ncl, BN, CL, rank);
-      } else {
-        const int z = blockIdx.x + (i - nprod) * (int)gridDim.x;
-        if (z >= H.zero_tiles) break;
-        tl = decode_zero_tile(P, z, BN);
-      }
+    for (int i = 0; i < nprod; ++i) {
+      const Tile tl = decode_tile(P, cid + i * ncl, BN, CL, rank);
       const GemmProblem& pr = H.prob[tl.p];
-      const int m = tl.m0 + 32 * g + lane;
-      const bool row_ok = m < pr.M;
-      long long row_off = 0;
-      if (row_ok)
-        row_off = (long long)(m / pr.rows_per_group) * pr.s_group_row +
-                  (long long)(m % pr.rows_per_group) * pr.s_row;
-      if (tl.zero) {  // rows with nothing to multiply: zeros
-        if (!row_ok) continue;
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = 0u;
-        for (int c = 0; c < BN && tl.n0 + c < pr.N; c += 32) store_row32(pr, row_off, tl.n0 + c, pk);
-        continue;
-      }
+      const int m0w = tl.m0 + 32 * g;
+      const long long ro = m0w + lane < pr.M ? row_offset(pr, m0w + lane) : 0;
       const uint32_t buf = tile_i & 1;
       const uint32_t phase = (tile_i >> 1) & 1;
       ++tile_i;
       if (!ok || !mbar_wait(&acc_full[buf], phase, w)) {
         ok = false;
-        continue;  // the zero fills after the product tiles still run
+        break;
       }
       tc_fence_after();
       const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(32 * g) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c, r);
+      for (int c = 0; c < BN; c += 64) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(taddr + c, r0);
+        tmem_ld32(taddr + c + 32, r1);
         tmem_wait_ld();
-        const int n = tl.n0 + c;
-        if (!row_ok || n >= pr.N) continue;
-        uint32_t pk[16];
+        // this lane's row, columns [c, c + 64): 8 chunks of 8 bf16
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-        store_row32(pr, row_off, n, pk);
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t* src = k < 4 ? r0 + 8 * k : r1 + 8 * (k - 4);
+          st[lane * 8 + (k ^ (lane & 7))] =
+              make_uint4(pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                         pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                         pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                         pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7])));
+        }
+        __syncwarp();
+        store_warp_rows(pr, st, m0w, ro, tl.n0 + c, false, lane);
+        __syncwarp();  // the staging area is rewritten by the next chunk
       }
       tc_fence_before();
       __syncwarp();
