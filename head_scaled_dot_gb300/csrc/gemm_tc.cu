@@ -66,17 +66,22 @@ struct GemmTcParams {
 
 constexpr int SMALL_RUNS = 8;
 
-template <int BN>
+// CL = 1: one CTA, a 128 x BN tile, A and the whole W tile in its shared
+// memory. CL = 2: a CTA pair computes a 256 x BN tile with cta_group::2
+// MMAs; each CTA holds its 128 rows of A and half of the W tile, so a stage
+// is smaller and the ring deeper in the same shared memory.
+template <int BN, int CL>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-  static constexpr int B_BYTES = BK * BN * 2;   // 32 KB (BN = 256)
+  static constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+  static constexpr int B_BYTES = BK * (BN / CL) * 2;  // this CTA's part of the W tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // epilogue staging: per epilogue warp 32 rows x 64 columns of bf16
   static constexpr int STAGING_BYTES = 4 * 32 * 128;
-  static constexpr int SMEM =
-      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int BUDGET = 227 * 1024 - STAGING_BYTES - 1024 /*align*/ - 256 /*barriers*/;
+  static constexpr int STAGES = BUDGET / STAGE_BYTES > 8 ? 8 : BUDGET / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // double-buffered accumulator
+  static_assert(STAGES >= 4, "shared memory");
 };
 
 // The k-th panel of a run table (runs sorted, k below the table's total).
@@ -181,16 +186,20 @@ __device__ __forceinline__ void store_warp_rows(const GemmProblem& pr, const uin
   }
 }
 
-// CL = 2: the kernel runs in clusters of two CTAs that compute vertically
-// adjacent tiles with the same N tile. Each CTA loads its own A panel and
-// half of the W tile, multicast into both CTAs' shared memory, so the W
-// tile is read from L2 once per pair; a stage is refilled only after both
-// CTAs' MMAs are done with it (their commits arrive on both CTAs' empty
-// barriers).
+// CL = 2: the kernel runs in clusters of two CTAs that compute a 256 x BN
+// tile (two vertically adjacent M panels, the same N tile) with cta_group::2
+// MMAs issued by one thread of the even CTA. Each CTA loads its own A panel
+// and its half of the W tile into its own shared memory (the W tile is read
+// from L2 once per pair, and a stage is 32 KB instead of 48 KB, so the ring
+// is six stages deep instead of four); the bytes of both CTAs complete on the
+// even CTA's full barrier, the issuer's commits arrive on both CTAs' empty
+// and accumulator barriers, and each CTA's epilogue reads its 128 rows of the
+// accumulator from its own tensor memory and frees it on the issuer's
+// barrier.
 template <int BN, int RUNS, int CL>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ GemmTcParams<RUNS> P) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, CL>;
   const GemmTcHead& H = P.h;
   const int rank = CL > 1 ? (int)cluster_rank() : 0;
   const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;  // cluster and clusters
@@ -208,12 +217,12 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);  // one MMA commit per CTA of the cluster
+      mbar_init(&full[s], 1);   // the (even CTA's) producer; the bytes of both CTAs
+      mbar_init(&empty[s], 1);  // one MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[b], 4 * CL);  // one arrival per epilogue warp of the pair
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -232,12 +241,17 @@ __global__ void __launch_bounds__(192, 1)
     if (cid < prod) first = decode_tile(P, cid, BN, CL, rank);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if (CL == 1) {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  // the other CTA's barriers are initialized before anything is multicast
+  // the other CTA's barriers are initialized before either signals them
   if (CL > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -263,36 +277,42 @@ __global__ void __launch_bounds__(192, 1)
           }
           uint8_t* a_s = smem + s * C::STAGE_BYTES;
           uint8_t* b_s = a_s + C::A_BYTES;
-          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          tma_load_2d(a_s, &H.amap[tl.p], &full[s], kb * BK, tl.m0);
           if (CL == 1) {
+            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+            tma_load_2d(a_s, &H.amap[tl.p], &full[s], kb * BK, tl.m0);
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
               tma_load_2d(b_s + j * (BK * 128), &H.bmap[tl.p], &full[s], tl.n0 + 64 * j, kb * BK);
           } else {
-            // this CTA's share of the W tile, into both CTAs
+            // this CTA's A panel and its half of the W tile, into its own
+            // shared memory; the bytes of both CTAs complete on the even
+            // CTA's full barrier, which expects them all
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], CL * C::STAGE_BYTES);
+            const uint32_t fb = cluster_addr(&full[s], 0);
+            tma_load_2d_pair(a_s, &H.amap[tl.p], fb, kb * BK, tl.m0);
             constexpr int PER = BN / 64 / CL;
 #pragma unroll
-            for (int j = rank * PER; j < (rank + 1) * PER; ++j)
-              tma_load_2d_mc(b_s + j * (BK * 128), &H.bmap[tl.p], &full[s], tl.n0 + 64 * j,
-                             kb * BK, (uint16_t)((1u << CL) - 1));
+            for (int j = 0; j < PER; ++j)
+              tma_load_2d_pair(b_s + j * (BK * 128), &H.bmap[tl.p], fb,
+                               tl.n0 + 64 * (rank * PER + j), kb * BK);
           }
         }
       }
-      if (!ok) {  // let the loads this CTA started land before it exits
+      if (!ok && rank == 0) {  // let the loads of this stage ring land before it exits
         for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
           drain_wait(&full[k % C::STAGES], (k / C::STAGES) & 1);
       }
       if (CL > 1) {
-        // the other CTA's last commits arrive on this CTA's empty barriers:
+        // the even CTA's last commits arrive on this CTA's empty barriers:
         // they must have landed before this CTA's shared memory is released
         for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
           drain_wait(&empty[k % C::STAGES], (k / C::STAGES) & 1);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 1);
+    // the MMA issuer: every CTA (CL = 1) or the even CTA of a pair
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM * CL, BN, 0, 1);
       uint32_t it = 0, tile_i = 0;
       bool ok = true;
       for (int t = cid; t < prod && ok; t += ncl, ++tile_i) {
@@ -321,20 +341,30 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t ad = sdesc_sw128(a_addr + kk * 32, 16, 1024);
             // B MN-major: 16 K-rows of 128 B each; 64-column panels 8 KB apart.
             const uint64_t bd = sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024);
-            umma_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            if (CL == 1)
+              umma_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            else
+              umma_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
           }
-          // frees the stage once these MMAs finish (in every CTA of the cluster,
-          // whose W halves it holds)
+          // frees the stage (in both CTAs of a pair) once these MMAs finish
           if (CL == 1)
             umma_commit(&empty[s]);
           else
-            umma_commit_mc(&empty[s], (uint16_t)((1u << CL) - 1));
+            umma_commit_pair_mc(&empty[s], 3);
         }
-        if (ok) umma_commit(&acc_full[buf]);
+        if (ok) {
+          if (CL == 1)
+            umma_commit(&acc_full[buf]);
+          else
+            umma_commit_pair_mc(&acc_full[buf], 3);
+        }
       }
       if (!ok) {  // wait for this thread's MMAs before TMEM is released
         uint64_t* last = &acc_full[0];
-        umma_commit(last);
+        if (CL == 1)
+          umma_commit(last);
+        else
+          umma_commit_pair_mc(last, 1);
         drain_wait(last, 0);
         drain_wait(last, 1);
       }
@@ -393,7 +423,12 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) {
+        if (CL == 1)
+          mbar_arrive(&acc_empty[buf]);
+        else
+          mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0));  // the issuer's barrier
+      }
     }
   }
   // Every lane of a warp meets here before the CTA-wide barrier: a barrier
@@ -405,7 +440,10 @@ __global__ void __launch_bounds__(192, 1)
   if (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    if (CL == 1)
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    else
+      tmem_dealloc_pair(tmem, C::TMEM_COLS);
   }
 }
 
@@ -423,7 +461,7 @@ int max_clusters() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL * (num_sms() / CL));
     cfg.blockDim = dim3(192);
-    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<BN, CL>::SMEM;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
@@ -439,9 +477,17 @@ int max_clusters() {
   return cached[dev];
 }
 
+// Clusters of the paired kernel that fit at once (0 if its shared memory
+// cannot be granted).
+template <int BN>
+int pair_clusters() {
+  if (!ensure_smem_limit((const void*)gemm_tc_kernel<BN, SMALL_RUNS, 2>, Cfg<BN, 2>::SMEM)) return 0;
+  return max_clusters<BN, SMALL_RUNS, 2>();
+}
+
 template <int BN, int RUNS, int CL>
 mha_status launch_kernel(const GemmTcParams<RUNS>& P, int clusters, cudaStream_t s) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, CL>;
   auto kernel = gemm_tc_kernel<BN, RUNS, CL>;
   if (!ensure_smem_limit((const void*)kernel, C::SMEM)) return MHA_ERR_CUDA;
   const int cap = max_clusters<BN, RUNS, CL>();
@@ -618,19 +664,27 @@ mha_status gemm_tc(const GemmProblem* probs, int nprob, const RowSelect* sel, in
       H.zero_prob = 0;
     }
   }
-  // Pairs of CTAs share the W tile (multicast) for the grouped projections
-  // with many tiles (measured on GB300: 4-11 % faster there; no gain for a
-  // single problem or a few hundred tiles, where the pair's lockstep costs
-  // what the halved W reads save).
+  // CTA pairs (256-row tiles, half of the W tile in each CTA's shared
+  // memory, a deeper ring) when their rounds over the clusters that fit at
+  // once are not more than the single CTAs' rounds over the SMs by the ~8 %
+  // a paired tile is faster by (measured on GB300: 3-7 % on the grouped
+  // projections; an output projection whose tiles fill whole rounds of
+  // single CTAs but not of pairs was 6 % slower in pairs).
   const int bn = all256 ? 256 : 128;
-  long long tiles = 0;
+  long long tiles = 0, pair_tiles = 0;
   for (int g = 0; g < H.ngroups; ++g) {
     long long nt = 0;
     for (int p = H.g_first[g]; p < H.g_first[g + 1]; ++p) nt += (probs[p].N + bn - 1) / bn;
     const GemmProblem& pr = probs[H.g_first[g]];
-    tiles += (H.g_select[g] ? sel_panels : (pr.M + BM - 1) / BM) * nt;
+    const long long panels = H.g_select[g] ? sel_panels : (pr.M + BM - 1) / BM;
+    tiles += panels * nt;
+    pair_tiles += (panels + 1) / 2 * nt;
   }
-  const bool pair = nprob > 1 && tiles >= 4LL * num_sms();
+  const int sms = num_sms();
+  const int clusters = all256 ? pair_clusters<256>() : pair_clusters<128>();
+  const long long rounds = (tiles + sms - 1) / sms;
+  const long long pair_rounds = clusters > 0 ? (pair_tiles + clusters - 1) / clusters : rounds + 1;
+  const bool pair = pair_rounds * 100 <= rounds * 108;
   if (!pair)
     return all256 ? launch<256, 1>(P, nprob, sel_panels, unsel_panels, s)
                   : launch<128, 1>(P, nprob, sel_panels, unsel_panels, s);

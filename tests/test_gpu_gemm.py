@@ -158,8 +158,9 @@ def test_general_form_three_inputs_three_groups():
     (3, 512, None, True),                 # cross: K and V over 1536 rows of X_kv per item
 ])
 def test_qkv_projection_in_cta_pairs_exact_on_integers(B, T, lens, cross):
-    """Grouped projections with more tiles than four per SM run in pairs of
-    CTAs that share the W tile (multicast). Small integers are exact in bf16
+    """Grouped projections with many tiles run in pairs of CTAs (one 256-row
+    tile, cta_group::2 MMAs, each CTA holding half of the W tile). Small
+    integers are exact in bf16
     and in the fp32 accumulator, so Q, K and V must match bit for bit, also
     for a pair whose second panel is past the last one and with only the
     selected panels of a padding mask computed."""
