@@ -46,8 +46,10 @@ struct DecodeParams {
   float cl2;       // c * log2(e)
   int causal_tail; // row i sees keys j <= L - n_q + i
   int valid_len[MHA_MAX_PADDED_BATCH];
-  // work items of the streaming kernel: (batch item, head, chunk), numbered
-  // batch item by batch item; item_start[b] = first item of batch item b
+  // the streaming kernel's work: the 32-key groups of every (batch item,
+  // head) key sequence, numbered batch item by batch item, head by head;
+  // item_start[b] = first group of batch item b, nitems = all groups. CTA c
+  // of G takes groups [c nitems / G, (c + 1) nitems / G).
   int nitems;
   int item_start[MHA_MAX_PADDED_BATCH + 1];
   // summaries per DEC_CHUNK keys: DEC_WARPS (one per warp of pass 1), or 1
@@ -487,20 +489,47 @@ struct DsCfg {
       DS_STAGES * STAGE + 2 * Q_FLOATS * 4 + 2 * DS_STAGES * 8 + 16 + COMBINE_FLOATS * 4;
 };
 
-// Batch item, head and chunk of work item `it`.
-__device__ __forceinline__ void ds_item(const DecodeParams& P, int it, int& b, int& head,
-                                        int& chunk) {
+constexpr int DS_GROUP = 32;                       // keys per group (one per lane)
+constexpr int DS_CHUNK_GROUPS = DEC_CHUNK / DS_GROUP;  // groups per summary chunk
+static_assert(DEC_CHUNK % DS_GROUP == 0, "chunk of whole groups");
+
+// A piece of a CTA's group range: keys [k0, k1) of the (b, head) sequence,
+// inside one chunk. Its summary goes to slot 2 chunk (the piece that starts
+// the chunk) or 2 chunk + 1 (the rest of a chunk that a range boundary cut);
+// a piece that is its whole chunk also marks slot 2 chunk + 1 empty. Every
+// range holds at least a chunk's worth of groups, so no chunk has more than
+// two pieces.
+struct DsPiece {
+  int b, head, chunk, k0, k1, slot;
+  bool clear_rest;
+};
+
+// The next piece from group g (advanced past it) of a range ending at g_end.
+__device__ __forceinline__ bool ds_next_piece(const DecodeParams& P, int& g, int g_end,
+                                              DsPiece& pc) {
+  if (g >= g_end) return false;
   int lo = 0, hi = P.B - 1;
-  while (lo < hi) {  // last b with item_start[b] <= it
+  while (lo < hi) {  // last b with item_start[b] <= g
     const int mid = (lo + hi + 1) >> 1;
-    if (P.item_start[mid] <= it) lo = mid;
+    if (P.item_start[mid] <= g) lo = mid;
     else hi = mid - 1;
   }
-  b = lo;
-  const int local = it - P.item_start[b];
-  const int nch = (P.valid_len[b] + DEC_CHUNK - 1) / DEC_CHUNK;
-  head = local / nch;
-  chunk = local % nch;
+  const int L = P.valid_len[lo];
+  const int ng = (L + DS_GROUP - 1) / DS_GROUP;  // groups of one head's sequence
+  const int local = g - P.item_start[lo];
+  const int gi = local % ng;
+  pc.b = lo;
+  pc.head = local / ng;
+  pc.chunk = gi / DS_CHUNK_GROUPS;
+  const int cstart = pc.chunk * DS_CHUNK_GROUPS;
+  const int cend = min(ng, cstart + DS_CHUNK_GROUPS);
+  const int len = min(cend - gi, g_end - g);
+  pc.k0 = gi * DS_GROUP;
+  pc.k1 = min(L, (gi + len) * DS_GROUP);
+  pc.slot = 2 * pc.chunk + (gi == cstart ? 0 : 1);
+  pc.clear_rest = gi == cstart && gi + len == cend;
+  g += len;
+  return true;
 }
 
 // A bounded wait that ignores the abort flag: used only while draining copies
@@ -542,6 +571,9 @@ __global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
   // until this grid has completed and its summaries are visible
   grid_dep_launch_dependents();
   const WaitCtl w{nullptr, abort_flag, P.limit_ns};
+  // this CTA's groups (an equal share of all keys, whatever the lengths)
+  const int g_begin = (int)((long long)blockIdx.x * P.nitems / gridDim.x);
+  const int g_end = (int)((long long)(blockIdx.x + 1) * P.nitems / gridDim.x);
   const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(P.K);
   const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(P.V);
 
@@ -550,11 +582,11 @@ __global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
       // producer: group n of this CTA's sequence goes to stage n % DS_STAGES
       uint32_t n = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < P.nitems && ok; it += gridDim.x) {
-        int b, head, chunk;
-        ds_item(P, it, b, head, chunk);
-        const int k0 = chunk * DEC_CHUNK, k1 = min(P.valid_len[b], k0 + DEC_CHUNK);
-        const long long row0 = ((long long)b * P.h + head) * P.n_k;
+      int g = g_begin;
+      DsPiece pc;
+      while (ok && ds_next_piece(P, g, g_end, pc)) {
+        const int k0 = pc.k0, k1 = pc.k1;
+        const long long row0 = ((long long)pc.b * P.h + pc.head) * P.n_k;
         for (int k = k0; k < k1; k += 32, ++n) {
           const int s = n % DS_STAGES;
           if (n >= (uint32_t)DS_STAGES &&
@@ -578,13 +610,13 @@ __global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
     const float cl2 = P.cl2;
     uint32_t n = 0;
     bool ok = true;
-    int ik = 0;  // items of this CTA so far
-    for (int it = blockIdx.x; it < P.nitems; it += gridDim.x, ++ik) {
-      int b, head, chunk;
-      ds_item(P, it, b, head, chunk);
-      const int L = P.valid_len[b];
-      const int k0 = chunk * DEC_CHUNK, k1 = min(L, k0 + DEC_CHUNK);
-      const long long bh = (long long)b * P.h + head;
+    int ik = 0;  // pieces of this CTA so far
+    int g = g_begin;
+    DsPiece pc;
+    for (; ds_next_piece(P, g, g_end, pc); ++ik) {
+      const int L = P.valid_len[pc.b];
+      const int k0 = pc.k0, k1 = pc.k1;
+      const long long bh = (long long)pc.b * P.h + pc.head;
       // the item's query rows, pre-multiplied by c log2(e), shared by the
       // consumer warps (double-buffered: a warp can only get here once every
       // warp has passed the previous item's barrier, i.e. has finished the
@@ -698,9 +730,9 @@ __global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
       }
-      // The item's summary of each row: the merge of the warps' summaries
-      // (those that took no group are empty), combined through shared memory,
-      // one per chunk. Split `chunk` of the row.
+      // The piece's summary of each row: the merge of the warps' summaries
+      // (those that took no group are empty), combined through shared
+      // memory, into the piece's slot of the row.
 #pragma unroll 1
       for (int r = 0; r < P.n_q && r < NQ; ++r) {
         constexpr int NT = 32 * DS_WARPS;
@@ -727,12 +759,17 @@ __global__ void __launch_bounds__(DS_THREADS, 1) decode_stream_kernel(
             for (int t = 0; t < CPL; ++t) cz[warp * D + lane * CPL + t] = z_run[rr][t] * wgt;
           }
         asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-        float* dst = P.part + ((bh * P.n_q + r) * P.nsplit + chunk) * (long long)(2 + D);
+        float* dst = P.part + ((bh * P.n_q + r) * P.nsplit + pc.slot) * (long long)(2 + D);
         for (int c = threadIdx.x; c < D; c += NT) {
           float zc = 0.f;
 #pragma unroll
           for (int i = 0; i < DS_WARPS; ++i) zc += cz[i * D + c];
           dst[2 + c] = zc;
+          if (pc.clear_rest) dst[(2 + D) + 2 + c] = 0.f;  // the chunk's second slot: empty
+        }
+        if (pc.clear_rest && threadIdx.x == 0) {
+          dst[(2 + D)] = -INFINITY;
+          dst[(2 + D) + 1] = 0.f;
         }
         if (threadIdx.x == 0) {
           float l = 0.f;
@@ -851,7 +888,10 @@ bool launch_stream(const DecodeParams& P, cudaStream_t s) {
   // asked once per device
   const int per_sm = resident_ctas((const void*)decode_stream_kernel<NQ, D>, DS_THREADS, C::SMEM);
   const int cap = num_sms() * per_sm;
-  const int grid = P.nitems < cap ? P.nitems : cap;
+  // at least a chunk's worth of groups per CTA (so a chunk has at most two
+  // pieces)
+  const int want = P.nitems / DS_CHUNK_GROUPS;
+  const int grid = want < 1 ? 1 : (want < cap ? want : cap);
   decode_stream_kernel<NQ, D><<<grid, DS_THREADS, C::SMEM, s>>>(P);
   return true;
 }
@@ -868,17 +908,17 @@ template <typename T>
 mha_status launch_decode(DecodeParams& P, int nchunk, cudaStream_t s) {
   const dim3 g1(nchunk, P.h, P.B), g2(P.n_q, P.h, P.B);
   if (sizeof(T) == 2 && P.d_h == P.d_vh && (P.d_h == 64 || P.d_h == 128) && P.n_q <= 8) {
-    // streaming pass 1: work items (batch item, head, chunk), batch item by
-    // batch item
-    long long items = 0;
+    // streaming pass 1: the 32-key groups of every (batch item, head)
+    // sequence, batch item by batch item, shared out in equal ranges
+    long long groups = 0;
     for (int b = 0; b < P.B; ++b) {
-      P.item_start[b] = (int)items;
-      items += (long long)P.h * ((P.valid_len[b] + DEC_CHUNK - 1) / DEC_CHUNK);
+      P.item_start[b] = (int)groups;
+      groups += (long long)P.h * ((P.valid_len[b] + DS_GROUP - 1) / DS_GROUP);
     }
-    if (items < (1ll << 30)) {
-      P.item_start[P.B] = (int)items;
-      P.nitems = (int)items;
-      P.per_chunk = 1;  // the streaming kernel writes one summary per chunk
+    if (groups < (1ll << 30)) {
+      P.item_start[P.B] = (int)groups;
+      P.nitems = (int)groups;
+      P.per_chunk = 2;  // two summary slots per chunk (a range boundary may cut it)
       const bool ok = P.d_h == 64 ? launch_stream_rows<64>(P, s) : launch_stream_rows<128>(P, s);
       if (!ok) return MHA_ERR_CUDA;
       // the merge follows pass 1 without a launch gap
