@@ -119,10 +119,12 @@ struct ACfg {
   static constexpr int K_BYTES = BLK_N * DQK * 2;
   static constexpr int V_BYTES = BLK_N * DV * 2;
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-  static constexpr int BUDGET = 227 * 1024 - 2 * Q_TILE_BYTES - 1024 - EXTRA;
+  // epilogue staging: each of the 8 softmax warps, 16 rows of DV bf16
+  static constexpr int STAGING = 8 * 16 * DV * 2;
+  static constexpr int BUDGET = 227 * 1024 - 2 * Q_TILE_BYTES - 1024 - EXTRA - STAGING;
   static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 4 ? 4 : (BUDGET / STAGE_BYTES);
   static constexpr int Q_BUFS = 1;  // Q tile pairs in shared memory
-  static constexpr int SMEM = 2 * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA;
+  static constexpr int SMEM = 2 * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA + STAGING;
   // TMEM columns: S of tile 0 and 1, then z (O) of tile 0 and 1.
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + DV;
@@ -431,6 +433,35 @@ __device__ void split_finish(const AttnTcParams& P, const Unit& u, int t, int r,
   }
 }
 
+// Epilogue stores through a warp's staging area in shared memory: its 16
+// rows of a tile, DV bf16 columns each (row rho at rho DV / 8 16-byte
+// chunks; chunk c at position c ^ (rho % 8), so that neither the lanes'
+// writes of their own rows nor the row-wise reads meet on a bank). Each lane
+// first stages the chunks of its half row; each store instruction then
+// writes 32 / (DV / 8) whole rows of the head's columns, contiguous in Z.
+template <int DV>
+__device__ __forceinline__ void stage_chunk(uint4* st, int rho, int c, uint4 v) {
+  st[rho * (DV / 8) + (c ^ (rho & 7))] = v;
+}
+
+// Stores the warp's staged rows q0w + rho (rho < 16) below n_q, columns below
+// dv; zrow0: the head's first column in row q0w of Z.
+template <int DV>
+__device__ __forceinline__ void store_staged_rows(const uint4* st, __nv_bfloat16* zrow0,
+                                                  long long row_stride, int q0w, int n_q,
+                                                  int dv, int lane) {
+  constexpr int CPR = DV / 8;     // chunks per row
+  constexpr int RPI = 32 / CPR;   // rows per store instruction
+  const int c = lane % CPR;
+#pragma unroll
+  for (int it = 0; it < 16 / RPI; ++it) {
+    const int rho = it * RPI + lane / CPR;
+    if (q0w + rho < n_q && 8 * c < dv)
+      *reinterpret_cast<uint4*>(zrow0 + (long long)rho * row_stride + 8 * c) =
+          st[rho * CPR + (c ^ (rho & 7))];
+  }
+}
+
 template <int DQK, int DV, bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ AttnTcParams P) {
@@ -457,6 +488,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* o_empty = o_full + 2;           // [2] per tile: z read out by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint4* staging = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(bars) + EXTRA);
   volatile int* split_flag = abort_flag + 1;  // the last split of a tile merges
 
   if (threadIdx.x == 0) {
@@ -803,29 +835,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         const bool computed = q < u.q_end;
         const float inv = computed ? (P.has_gate ? P.head_gate[u.head] : 1.f) / l_tot : 0.f;
+        uint4* st = staging + (warp - 4) * (16 * DV / 8);
 #pragma unroll
         for (int cb = 0; cb < DV / 64; ++cb) {
           uint32_t o[32];
           tmem_ld_x2_32<DV / 2>(o_addr + 32 * cb, o);
           tmem_wait_ld();
-          if (q < P.n_q) {
-            uint32_t pk[16];
+          uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[j] = computed ? pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
-                                             __uint_as_float(o[2 * j + 1]) * inv)
-                               : 0u;
-            uint4* dst = reinterpret_cast<uint4*>(zrow + 32 * cb);
-            // columns past d_vh (V was read as zeros there) are not written
+          for (int j = 0; j < 16; ++j)
+            pk[j] = computed ? pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
+                                           __uint_as_float(o[2 * j + 1]) * inv)
+                             : 0u;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (half * (DV / 2) + 32 * cb + 8 * j < P.dv)
-                dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-          }
+          for (int j = 0; j < 4; ++j)
+            stage_chunk<DV>(st, lane & 15, (half * (DV / 2) + 32 * cb) / 8 + j,
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&o_empty[t]);
+        if (lane == 0) mbar_arrive(&o_empty[t]);  // z is read: the next unit may overwrite it
+        // the warp's rows, row by row (columns past d_vh, read as zeros from
+        // V, are not written)
+        const int q0w = u.q0 + t * BLK_M + 32 * g + 16 * hh;
+        store_staged_rows<DV>(st, Zg + zbase + (long long)q0w * zrow_stride, zrow_stride, q0w,
+                              P.n_q, P.dv, lane);
+        __syncwarp();  // the staging area is rewritten by the next tile
       }
     }
   }
@@ -861,14 +896,17 @@ struct SpCfg {
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
   // barriers (up to 64 x 8 B)
   static constexpr int EXTRA_SP = 512;
+  // epilogue staging: each of the 16 softmax warps, 16 rows of 64 bf16
+  static constexpr int STAGING = 16 * 16 * 64 * 2;
   // a second pair of Q tiles (the next unit's, loaded while the current one
   // runs) where it leaves the ring at four stages
   static constexpr int Q_BUFS =
-      (227 * 1024 - 4 * Q_TILE_BYTES - 1024 - EXTRA_SP) / STAGE_BYTES >= 4 ? 2 : 1;
-  static constexpr int BUDGET = 227 * 1024 - 2 * Q_BUFS * Q_TILE_BYTES - 1024 - EXTRA_SP;
+      (227 * 1024 - 4 * Q_TILE_BYTES - 1024 - EXTRA_SP - STAGING) / STAGE_BYTES >= 4 ? 2 : 1;
+  static constexpr int BUDGET =
+      227 * 1024 - 2 * Q_BUFS * Q_TILE_BYTES - 1024 - EXTRA_SP - STAGING;
   static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 4 ? 4 : (BUDGET / STAGE_BYTES);
   static constexpr int SMEM =
-      2 * Q_BUFS * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA_SP;
+      2 * Q_BUFS * Q_TILE_BYTES + STAGES * STAGE_BYTES + 1024 + EXTRA_SP + STAGING;
   // TMEM columns of tile t: S at 128 t, P at 256 + 64 t, z at 384 + 64 t
   static constexpr uint32_t S_COL = 0, P_COL = 256, O_COL = 384;
   static_assert(STAGES >= 2, "shared memory");
@@ -902,6 +940,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   uint64_t* o_empty = o_full + 2;           // [2] z read out by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint4* staging = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(bars) + C::EXTRA_SP);
   volatile int* split_flag = abort_flag + 1;  // [2]: the last split of a tile merges
 
   if (threadIdx.x == 0) {
@@ -1217,21 +1256,26 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       uint32_t o[32];
       tmem_ld_x2_32<32>(o_addr, o);
       tmem_wait_ld();
-      if (q < P.n_q) {
+      uint4* st = staging + (warp - 4) * (16 * DV / 8);
+      {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           pk[j] = computed ? pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
                                          __uint_as_float(o[2 * j + 1]) * inv)
                            : 0u;
-        uint4* dst = reinterpret_cast<uint4*>(zrow);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          stage_chunk<DV>(st, lane & 15, 4 * half + j,
+                          make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_empty[t]);
+      if (lane == 0) mbar_arrive(&o_empty[t]);  // z is read: the next unit may overwrite it
+      const int q0w = tq0 + r - (lane & 15);     // the warp's first row
+      store_staged_rows<DV>(st, zrow - 32 * half - (long long)(lane & 15) * zrow_stride,
+                            zrow_stride, q0w, P.n_q, DV, lane);
+      __syncwarp();  // the staging area is rewritten by the next tile
     }
   }
   __syncwarp();
