@@ -64,6 +64,7 @@
 
 #include <algorithm>
 #include <functional>
+#include <mutex>
 #include <vector>
 
 #include "device_common.cuh"
@@ -1549,6 +1550,61 @@ int plan_call(AttnTcParams& P, const AttnArgs& a, int G) {
   return choose_schedule(P, a.B, a.d_h, a.d_vh, G, max_split);
 }
 
+// The schedule of the last few (shape, lengths, SM count, split request)
+// seen, so that repeated calls skip the host simulation (up to ~0.2 ms per
+// call on a large causal problem). Any schedule plan_call returns for a
+// shape covers every (query tile, key block) whatever the lengths, so a hash
+// collision of the lengths could only cost speed, never correctness.
+struct PlanKey {
+  int B, n_q, n_k, h, d_h, d_vh, causal, padding, pad_queries, G, nsplit, has_ws;
+  size_t ws_bytes;
+  uint64_t lens_hash;
+  bool operator==(const PlanKey& o) const {
+    return B == o.B && n_q == o.n_q && n_k == o.n_k && h == o.h && d_h == o.d_h &&
+           d_vh == o.d_vh && causal == o.causal && padding == o.padding &&
+           pad_queries == o.pad_queries && G == o.G && nsplit == o.nsplit &&
+           has_ws == o.has_ws && ws_bytes == o.ws_bytes && lens_hash == o.lens_hash;
+  }
+};
+
+struct PlanVal {
+  int grid, units, pair_units, pi_major, nsplit, split_blocks;
+};
+
+int cached_plan(AttnTcParams& P, const AttnArgs& a, int G) {
+  PlanKey k{a.B, a.n_q, a.n_k, a.h, a.d_h, a.d_vh, a.causal, a.padding, a.pad_queries, G,
+            a.nsplit, a.split_ws != nullptr, a.split_ws_bytes, 1469598103934665603ull};
+  if (a.padding)
+    for (int b = 0; b < a.B; ++b)  // FNV-1a over the lengths
+      k.lens_hash = (k.lens_hash ^ (uint32_t)a.valid_len_host[b]) * 1099511628211ull;
+  constexpr int N = 16;
+  static std::mutex mu;
+  static PlanKey keys[N];
+  static PlanVal vals[N];
+  static int used = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (keys[i] == k) {
+        const PlanVal& v = vals[i];
+        P.units = v.units;
+        P.pair_units = v.pair_units;
+        P.pi_major = v.pi_major;
+        P.nsplit = v.nsplit;
+        P.split_blocks = v.split_blocks;
+        return v.grid;
+      }
+  }
+  const int grid = plan_call(P, a, G);
+  if (grid < 0) return grid;
+  std::lock_guard<std::mutex> lock(mu);
+  keys[next] = k;
+  vals[next] = PlanVal{grid, P.units, P.pair_units, P.pi_major, P.nsplit, P.split_blocks};
+  next = (next + 1) % N;
+  if (used < N) ++used;
+  return grid;
+}
+
 }  // namespace
 
 size_t attention_split_bytes(int B, int n_q, int h, int d_vh, int nsplit) {
@@ -1647,7 +1703,7 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
     P.head_gate[i] = (P.has_gate && i < a.h) ? a.head_gate_host[i] : 1.f;
   // one CTA per unit, or one persistent CTA per SM walking its share; a
   // split over the keys when asked for, or when the tile pairs leave SMs idle
-  const int grid = plan_call(P, a, num_sms());
+  const int grid = cached_plan(P, a, num_sms());
   if (grid < 0) return MHA_ERR_WORKSPACE;
   if (P.nsplit > 1) {
     const size_t cnt_bytes = split_counter_bytes(P.npair * P.nbh);
