@@ -462,15 +462,17 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_partial_fast_kernel(
 // ---------------------------------------------------------------------------
 // Streaming pass 1 (bf16, d_h = d_vh = D in {64, 128}, up to 8 query rows).
 //
-// A persistent CTA walks work items (batch item, head, DEC_CHUNK-key chunk).
-// One producer thread copies each 32-key group of the cache, its K rows and
-// its V rows (contiguous in the head-split layout), into a DS_STAGES-deep
-// shared-memory ring with bulk asynchronous copies, as far ahead as the ring
-// allows and independently of the arithmetic, so that many groups' bytes are
-// in flight per SM. Consumer warp w takes groups n = w, w + DS_WARPS, ... of
-// the CTA's sequence, folds each into its own summary of the item's rows and
-// writes it as split chunk * DS_WARPS + w (an empty summary if it took no
-// group of the item), as decode_partial_kernel does.
+// One CTA per SM takes an equal contiguous range of the 32-key groups of all
+// (batch item, head) sequences and walks it piece by piece (a piece: its
+// groups of one DEC_CHUNK-key chunk of one sequence). One producer thread
+// copies each group of the cache, its K rows and its V rows (contiguous in the
+// head-split layout), into a DS_STAGES-deep shared-memory ring with bulk
+// asynchronous copies, as far ahead as the ring allows and independently of
+// the arithmetic, so that many groups' bytes are in flight per SM. Consumer
+// warp w takes groups n = w, w + DS_WARPS, ... of the CTA's sequence and folds
+// each into its own summary of the piece's rows; at the end of a piece the
+// warps' summaries are merged through shared memory and written once, into
+// the chunk's first or second slot (see DsPiece).
 // ---------------------------------------------------------------------------
 
 constexpr int DS_WARPS = DEC_WARPS;  // consumer warps: same split count as pass 1
