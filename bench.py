@@ -598,14 +598,20 @@ def run_reference(args):
 
 
 def kernel_rows(res, pk):
+    """Per kernel: the mean time of its launches (ms, the figure the rates
+    use), their median and best, the rate on the effective count and its
+    fraction of the measured bf16 peak (burst: the kernels are timed one by
+    one; and sustained, for reference)."""
     fl = res["flops"]
-    n = len(res["per"]["step"])
     rows = {}
     for name, key in (("qkv_projection", "qkv"), ("attention", "attention"),
                       ("output_projection", "out")):
-        ms = sum(res["per"][key]) / n
+        t = res["per"][key]
+        ms = sum(t) / len(t)
         tf = fl[key] / (ms * 1e-3) / 1e12
-        rows[name] = {"ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"]}
+        rows[name] = {"ms": ms, "ms_median": statistics.median(t), "ms_best": min(t),
+                      "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"],
+                      "frac_of_bf16_peak_sustained": tf / pk["bf16_tflops_sustained"]}
     return rows
 
 
@@ -740,6 +746,16 @@ def run_ours(args):
                           "ms_per_step": es_ms / args.steps,
                           "how": "copy in, forward, copy out, host read, one step at a time "
                                  "(L2 flushed before each step)"}}
+    # with padding the primary count above is the effective one (valid rows
+    # and keys only); the nominal count takes every row and key of the shapes
+    nominal = None
+    if res["lens"] is not None:
+        from head_scaled_dot_gb300 import workcount
+        nf = workcount.flops(w, None)["total"]
+        nominal = {"gflop_per_step": nf / 1e9,
+                   "tflops": world * nf * args.steps / (total_ms * 1e-3) / 1e12,
+                   "note": "dense count: all n_q rows and n_k keys of every batch item; the "
+                           "padded rows and keys are not computed"}
     if rank != 0:
         return
     line = {
@@ -753,6 +769,10 @@ def run_ours(args):
                               "steps that ends where the timed steps begin",
                        parallelism="replicas" if world > 1 else "single GPU"),
         "frac_of_bf16_peak": value / world / pk["bf16_tflops"],
+        "frac_of_bf16_peak_sustained": value / world / pk["bf16_tflops_sustained"],
+        "step_ms_median": statistics.median(res["per"]["step"]),
+        "step_ms_best": min(res["per"]["step"]),
+        "nominal": nominal,
         "roofline": roof,
         "kernels": krows,
         "cpu_baseline": cpu,

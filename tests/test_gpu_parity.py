@@ -425,3 +425,30 @@ def test_more_heads_than_gate_slots_without_a_gate(dtype, d):
     torch.cuda.synchronize()
     ref = oracle_attention_heads(Q, K, V, c, "causal", None, True)
     assert rel_err(f64(Z), ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("d", [(64, 64), (128, 128)])
+def test_schedule_of_one_shape_with_new_lengths(d):
+    """The host keeps the attention schedule of recent (shape, lengths)
+    calls. The same shape with other valid lengths (here every few calls,
+    returning to earlier lengths) must be computed for its own lengths: the
+    kernels read the lengths of the call, whatever schedule is reused."""
+    d_h, d_vh = d
+    B, h, n = 10, 4, 900
+    g = torch.Generator().manual_seed(900 + d_h)
+    Q = torch.randn((B, h, n, d_h), generator=g).bfloat16()
+    K = torch.randn((B, h, n, d_h), generator=g).bfloat16()
+    V = torch.randn((B, h, n, d_vh), generator=g).bfloat16()
+    c = 1 / math.sqrt(d_h)
+    sets = [[900, 1, 129, 256, 257, 500, 640, 641, 899, 384],
+            [300, 900, 900, 2, 700, 128, 513, 65, 900, 880],
+            [900] * 10]
+    Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+    for lens in sets + sets[:2]:
+        Z = mha.attention(Qd, Kd, Vd, c, "causal_padding", lens, self_attention=True)
+        torch.cuda.synchronize()
+        ref = oracle_attention_heads(Q, K, V, c, "causal_padding", lens, True)
+        got = f64(Z)
+        for b, L in enumerate(lens):
+            assert np.all(got[b, L:] == 0.0)
+        assert rel_err(got, ref) <= 1e-2, lens
