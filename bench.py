@@ -753,9 +753,10 @@ def run_ours(args):
         from head_scaled_dot_gb300 import workcount
         nf = workcount.flops(w, None)["total"]
         nominal = {"gflop_per_step": nf / 1e9,
-                   "tflops": world * nf * args.steps / (total_ms * 1e-3) / 1e12,
-                   "note": "dense count: all n_q rows and n_k keys of every batch item; the "
-                           "padded rows and keys are not computed"}
+                   "dense_equivalent_tflops": world * nf * args.steps / (total_ms * 1e-3) / 1e12,
+                   "note": "dense count: all n_q rows and n_k keys of every batch item. The "
+                           "padded rows and keys are not computed, so this rate is not "
+                           "achieved throughput (value, on the effective count, is)"}
     if rank != 0:
         return
     line = {
