@@ -87,6 +87,7 @@ def chosen_workload(args):
     from head_scaled_dot_gb300 import workloads
     if args.workload:
         named = {w.name: w for w in workloads.WORKLOADS + [workloads.GENERAL_DIMS,
+                                                           workloads.SMALL_DIMS,
                                                            workloads.SIMT_DIMS]
                  + workloads.LONG_KEYS}
         if args.workload not in named:
@@ -629,7 +630,7 @@ def roofline(w, krows, pk, pk_kind, dev):
     roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "peak_kind": pk_kind + " burst",
             "ms_per_launch": krows[dom]["ms"], "traffic": stored_traffic(dom, w.name)}
-    attn_cuda_cores = w.dtype == "f32" or not all(64 <= d <= 128 and d % 8 == 0
+    attn_cuda_cores = w.dtype == "f32" or not all(32 <= d <= 128 and d % 8 == 0
                                                   for d in (w.d_h, w.d_vh))
     if w.dtype == "f32" or (dom == "attention" and attn_cuda_cores):
         # the fp32 path, and attention of head sizes off the tensor cores, run
@@ -678,17 +679,19 @@ def run_ours(args):
                                "ms_per_step": r["total_ms"] / len(r["per"]["step"]),
                                "kernels": kr, "roofline": roofline(wj, kr, pk, pk_kind, dev)}
             del r
-        # general head sizes: d_h = 96 (bf16 heads of 64..128 run in the
-        # 128-wide tensor-core kernels) and d_h = 32 (the CUDA-core kernel,
-        # against the fp32 FMA peak); the flop count uses the head size itself
-        for gw in (workloads.GENERAL_DIMS, workloads.SIMT_DIMS):
+        # general head sizes: d_h = 96 (bf16 heads of 72..128 run in the
+        # 128-wide tensor-core kernels), d_h = 32 (heads of 32..64 in the
+        # 64-wide ones), d_h = 24 (the CUDA-core kernel, against the fp32 FMA
+        # peak); the flop count uses the head size itself
+        for gw in (workloads.GENERAL_DIMS, workloads.SMALL_DIMS, workloads.SIMT_DIMS):
             r = measure_workload(gw, max(3, args.steps // 2), 3, dev, 1, e2e=False,
                                  sample_clocks=False)
             kr = kernel_rows(r, pk)
-            on_tc = gw.dtype == "bf16" and all(64 <= d <= 128 and d % 8 == 0
+            on_tc = gw.dtype == "bf16" and all(32 <= d <= 128 and d % 8 == 0
                                                for d in (gw.d_h, gw.d_vh))
             if on_tc:
-                groof = {"kernel": "attention (tensor cores, head padded to 128)",
+                groof = {"kernel": "attention (tensor cores, head padded to %d)"
+                                   % (64 if max(gw.d_h, gw.d_vh) <= 64 else 128),
                          "bound": "tensor", "peak": pk["bf16_tflops"],
                          "peak_kind": pk_kind + " burst"}
             else:

@@ -920,7 +920,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   constexpr int DV = 64;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   __nv_bfloat16* Zg = static_cast<__nv_bfloat16*>(P.Z);
-  const long long zrow_stride = (long long)P.h * DV;
+  const long long zrow_stride = (long long)P.h * P.dv;  // d_vh <= 64 columns per head
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1211,13 +1211,15 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         if (lane == 0) mbar_arrive(&p_full[t]);
       }
       // Epilogue of the unit: z / l for this half of each row
-      __nv_bfloat16* zrow = Zg + (long long)u.b * P.n_q * zrow_stride + (long long)u.head * DV +
+      __nv_bfloat16* zrow = Zg + (long long)u.b * P.n_q * zrow_stride + (long long)u.head * P.dv +
                             (long long)q * zrow_stride + 32 * half;
       if (SPLIT ? !(t ? u.has1 : u.has0) : nblk == 0) {
         // the whole tile is padding: its rows are zero (written by split 0)
         if (q < P.n_q && u.split == 0) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
+          for (int j = 0; j < 4; ++j)
+            if (32 * half + 8 * j < P.dv)
+              reinterpret_cast<uint4*>(zrow)[j] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -1274,8 +1276,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[t]);  // z is read: the next unit may overwrite it
       const int q0w = tq0 + r - (lane & 15);     // the warp's first row
+      // (columns past d_vh, read as zeros from V, are not written)
       store_staged_rows<DV>(st, zrow - 32 * half - (long long)(lane & 15) * zrow_stride,
-                            zrow_stride, q0w, P.n_q, DV, lane);
+                            zrow_stride, q0w, P.n_q, P.dv, lane);
       __syncwarp();  // the staging area is rewritten by the next tile
     }
   }
@@ -1509,7 +1512,7 @@ mha_status set_units(AttnTcParams& P, const AttnArgs& a) {
   return MHA_OK;
 }
 
-int split_dv(int d_vh) { return d_vh == 64 ? 64 : 128; }
+int split_dv(int d_vh) { return d_vh <= 64 ? 64 : 128; }
 
 size_t split_counter_bytes(int pairs) {
   return ((size_t)pairs * 2 * sizeof(int) + 255) / 256 * 256;
@@ -1712,12 +1715,13 @@ mha_status attention_tc(const AttnArgs& a, cudaStream_t s) {
     if (!a.split_cnt_zeroed && cudaMemsetAsync(P.split_cnt, 0, cnt_bytes, s) != cudaSuccess)
       return MHA_ERR_CUDA;
   }
-  // Head sizes between 64 and 128 run as 128: the 64-wide panels past d_h
-  // (past d_vh) are read as zeros (TMA fill past the tensor's extent), so
-  // the padded dot products are exact and z's extra columns stay 0 and are
-  // not written. d_vh = 64: S, P and z fit in separate TMEM columns.
-  if (a.d_h < 64 || a.d_h > 128 || a.d_vh < 64 || a.d_vh > 128) return MHA_ERR_UNSUPPORTED;
-  const bool q64 = a.d_h == 64, v64 = a.d_vh == 64;
+  // Head sizes of 32..64 run as 64 and those of 72..128 as 128: the columns
+  // past d_h (past d_vh) of the 64-wide panels are read as zeros (TMA fill
+  // past the tensor's extent), so the padded dot products are exact and z's
+  // extra columns stay 0 and are not written. d_vh <= 64: S, P and z fit in
+  // separate TMEM columns.
+  if (a.d_h < 32 || a.d_h > 128 || a.d_vh < 32 || a.d_vh > 128) return MHA_ERR_UNSUPPORTED;
+  const bool q64 = a.d_h <= 64, v64 = a.d_vh <= 64;
   if (q64 && v64) return launch_sp<64>(P, grid, s);
   if (!q64 && !v64) return launch<128, 128>(P, grid, s);
   if (q64) return launch<64, 128>(P, grid, s);

@@ -191,7 +191,7 @@ Layout layout(int B, int n_q, int n_k, int h, int d_h, int d_vh, mha_dtype dt) {
   return L;
 }
 
-// Head sizes every path handles: 1 .. MAX_HEAD_DIM. bf16 heads of 64..128
+// Head sizes every path handles: 1 .. MAX_HEAD_DIM. bf16 heads of 32..128
 // (multiples of 8) run on the tensor cores, other sizes on the CUDA-core
 // kernel.
 constexpr int MAX_HEAD_DIM = 256;
@@ -206,7 +206,7 @@ mha_status check_head_dims(int d_h, int d_vh, mha_dtype dt) {
 // the 128-wide kernels (multiples of 8, as their tensor maps need 16-byte
 // strides).
 bool tc_head_dims(int d_h, int d_vh) {
-  auto ok = [](int d) { return d >= 64 && d <= 128 && d % 8 == 0; };
+  auto ok = [](int d) { return d >= 32 && d <= 128 && d % 8 == 0; };
   return ok(d_h) && ok(d_vh);
 }
 

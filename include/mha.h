@@ -143,9 +143,10 @@ MHA_API mha_status mha_workspace_layout(int B, int n_q, int n_k, int h, int d_h,
  *                                aligned; its contents on entry do not matter
  *
  * Head sizes d_h, d_vh from 1 to 256 (MHA_ERR_UNSUPPORTED otherwise); bf16
- * heads with d_h and d_vh in 64..128 and multiples of 8 run on the tensor
- * cores (sizes above 64 in the 128-wide kernels, the columns past d_h or d_vh
- * read as zeros), other sizes on CUDA cores.
+ * heads with d_h and d_vh in 32..128 and multiples of 8 run on the tensor
+ * cores (sizes of 32..64 in the 64-wide kernels, sizes above 64 in the
+ * 128-wide ones, the columns past d_h or d_vh read as zeros), other sizes on
+ * CUDA cores.
  * bf16 also needs d_model, d_h, d_vh and d_o to be multiples of 8.
  * When the bf16 tile pairs of the attention step are too few to fill the
  * GPU, the step splits the keys as mha_attention_split does with nsplit = 0,
@@ -190,8 +191,9 @@ MHA_API mha_status mha_forward(const void* X_q, const void* X_kv, const void* W_
  *                                any d_model: the intermediates do not depend
  *                                on the input widths)
  *
- * Head sizes d_h, d_vh from 1 to 256; bf16 heads with d_h and d_vh in 64..128
- * run on the tensor cores (as for mha_forward), other sizes on CUDA cores.
+ * Head sizes d_h, d_vh from 1 to 256; bf16 heads with d_h and d_vh in 32..128
+ * (multiples of 8) run on the tensor cores (as for mha_forward), other sizes
+ * on CUDA cores.
  * bf16 also needs d_q, d_k, d_v,
  * d_h, d_vh and d_o to be multiples of 8 and 16-byte aligned pointers
  * (MHA_ERR_UNSUPPORTED otherwise). Other errors as for mha_forward.
@@ -295,7 +297,7 @@ MHA_API mha_status mha_attention_split(const void* Q, const void* K, const void*
 
 /*
  * The schedule of the tensor-core attention for bf16 heads (d_h and d_vh in
- * 64..128, multiples of 8), computed on the host for a GPU with num_sms SMs;
+ * 32..128, multiples of 8), computed on the host for a GPU with num_sms SMs;
  * it launches nothing and needs no GPU. nsplit as for mha_attention_split:
  * 1 is the schedule of mha_attention, 0 that of mha_forward (the automatic
  * split with the scratch mha_workspace_size provides). A unit is one 128-row

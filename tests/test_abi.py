@@ -147,7 +147,7 @@ def test_split_attention_rejects_bad_arguments_on_host(lib):
                                        mask, None, 0, nsplit, dt, P(ws) if ws else None,
                                        ws_bytes, None, None)
     assert split(-1) == 1 and split(257) == 1                 # INVALID_ARG
-    assert split(4, dt=0) == 2 and split(4, d=32) == 2        # fp32 / off the tensor cores
+    assert split(4, dt=0) == 2 and split(4, d=24) == 2        # fp32 / off the tensor cores
     assert split(4, ws=None) == 4                              # WORKSPACE: missing,
     assert split(4, ws=(1 << 20) + 16) == 4                    # misaligned,
     assert split(4, ws_bytes=1000) == 4                        # too small

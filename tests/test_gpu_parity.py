@@ -337,7 +337,8 @@ GENERAL = [
     # B, n_q, n_k, d_q, d_k, d_v, h, d_h, d_vh, d_o, mask, self_attention, lens
     (2, 130, 200, 64, 96, 40, 3, 64, 64, 72, "padding", False, [1, 200]),   # tensor cores
     (2, 150, 150, 64, 64, 64, 2, 128, 64, 64, "causal", True, None),        # tensor cores
-    (2, 77, 140, 48, 32, 56, 3, 32, 48, 40, "none", False, None),          # CUDA cores
+    (2, 77, 140, 48, 32, 56, 3, 32, 48, 40, "none", False, None),          # tensor cores (as 64)
+    (2, 90, 90, 48, 48, 48, 3, 24, 16, 40, "causal_padding", True, [90, 30]),  # CUDA cores
     (1, 100, 100, 96, 96, 96, 2, 96, 96, 96, "causal_padding", True, [61]),  # tensor cores (bf16)
     (1, 70, 90, 256, 128, 64, 2, 256, 256, 64, "padding", False, [45]),     # d = 256
 ]

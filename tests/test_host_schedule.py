@@ -158,7 +158,7 @@ def test_split_workspace_sizes():
         256 + 16 * 2 * 10 * 130 * 128 * 4
     assert mha.attention_split_workspace_size(8, 2048, 2048, 16, 64, 64, 0) == 0
     # head sizes off the tensor cores never split
-    assert mha.attention_split_workspace_size(1, 128, 4096, 1, 32, 32, 4) == 0
+    assert mha.attention_split_workspace_size(1, 128, 4096, 1, 24, 24, 4) == 0
     # mha_forward's workspace includes the automatic split's scratch
     base = mha.workspace_size(2, 128, 32768, 1024, 8, 128, 128, 1024, "f32")
     assert mha.workspace_size(2, 128, 32768, 1024, 8, 128, 128, 1024, "bf16") >= \
@@ -182,7 +182,8 @@ def test_plan_rejects_what_attention_rejects():
     assert status(2, 256, 256, 4, 64, 64, num_sms=0) == 1            # INVALID_ARG
     assert status(2, 256, 128, 4, 64, 64, "causal", self_attention=False) == 1
     assert status(2, 256, 256, 4, 96, 64) == 0                        # 96 runs as 128
-    assert status(2, 256, 256, 4, 48, 64) == 2                        # UNSUPPORTED head sizes
+    assert status(2, 256, 256, 4, 48, 64) == 0                        # 48 runs as 64
+    assert status(2, 256, 256, 4, 24, 64) == 2                        # UNSUPPORTED head sizes
     assert status(2, 256, 256, 4, 64, 100) == 2
     assert status(2, 256, 256, 4, 136, 64) == 2
     assert status(2, 256, 256, 4, 64, 64, "padding", [0, 10]) == 3    # EMPTY_ROW
