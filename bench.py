@@ -699,7 +699,9 @@ def run_ours(args):
                          "peak": alu_peak_tflops(dev, sm_max_mhz()),
                          "peak_kind": "derived: SMs x 128 FP32 lanes x 2 flop x max SM clock"}
             groof.update(achieved=kr["attention"]["tflops"], unit="TFLOP/s",
-                         frac=kr["attention"]["tflops"] / groof["peak"])
+                         frac=kr["attention"]["tflops"] / groof["peak"],
+                         ms_per_launch=kr["attention"]["ms"],
+                         traffic=stored_traffic("attention", gw.name))
             others[gw.name] = {"tflops": r["flops"]["total"] * len(r["per"]["step"])
                                / (r["total_ms"] * 1e-3) / 1e12,
                                "ms_per_step": r["total_ms"] / len(r["per"]["step"]),

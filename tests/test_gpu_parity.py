@@ -48,9 +48,17 @@ def check_full(w, inp, Y):
 # The five workloads at full size
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("idx", [0, 1])
+NAMED = {"general_dims": workloads.GENERAL_DIMS, "small_dims": workloads.SMALL_DIMS,
+         "simt_dims": workloads.SIMT_DIMS}
+
+
+def workload(idx):
+    return NAMED[idx] if idx in NAMED else workloads.WORKLOADS[idx]
+
+
+@pytest.mark.parametrize("idx", [0, 1, "small_dims", "simt_dims"])
 def test_workload_full_compare(idx):
-    w = workloads.WORKLOADS[idx]
+    w = workload(idx)
     inp = workloads.make_inputs(w)
     check_full(w, inp, run(w, inp))
 
@@ -64,7 +72,7 @@ def sample_rows(w, L, rng, n=24):
 
 @pytest.mark.parametrize("idx", [2, 3, 4, "general_dims"])
 def test_workload_sampled_rows(idx):
-    w = workloads.GENERAL_DIMS if idx == "general_dims" else workloads.WORKLOADS[idx]
+    w = workload(idx)
     inp = workloads.make_inputs(w)
     got = f64(run(w, inp))
     assert np.isfinite(got).all()
@@ -84,7 +92,7 @@ def test_workload_sampled_rows(idx):
     assert worst <= TOL[w.dtype], "rel err %.3e" % worst
 
 
-@pytest.mark.parametrize("idx", [2, 3, 4, "general_dims"])
+@pytest.mark.parametrize("idx", [2, 3, 4, "general_dims", "small_dims", "simt_dims"])
 def test_workload_full_attention_step(idx):
     """Every element of Z at full size, in the launch configuration of the
     benchmark: the attention step on the GPU's own bf16 Q, K, V (from the
@@ -92,7 +100,7 @@ def test_workload_full_attention_step(idx):
     values, one (batch item, head) at a time. Padded query rows must be
     exactly zero; the metric is max|Z - Z_ref| / max|Z_ref| over the computed
     rows of the whole Z."""
-    w = workloads.GENERAL_DIMS if idx == "general_dims" else workloads.WORKLOADS[idx]
+    w = workload(idx)
     inp = workloads.make_inputs(w)
     t = to_dev(inp)
     lens = lens_list(inp)
