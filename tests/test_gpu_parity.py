@@ -145,6 +145,22 @@ def test_small_shapes(shape, dtype):
     check_full(w, inp, run(w, inp))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("mask", ["causal_padding", "padding"])
+def test_largest_padded_batch(mask, dtype):
+    """MHA_MAX_PADDED_BATCH (1024) batch items, each with its own valid length
+    (1 to 40 of 40 positions): the launch parameters' length tables are full,
+    and the GEMMs' zero-filled padding panels and the attention's units span
+    every batch item."""
+    B, T = 1024, 40
+    w = workloads.Workload(name="max_batch", B=B, n_q=T, n_k=T, d_model=64, h=1, d_h=64,
+                           d_vh=64, d_o=64, mask=mask, dtype=dtype, cross=False,
+                           c=1 / math.sqrt(64), seed=21)
+    lens = [1 + (37 * b) % T for b in range(B)]
+    inp = workloads.make_inputs(w, lengths=lens)
+    check_full(w, inp, run(w, inp))
+
+
 # c = 0.9 is 7x the usual 1/sqrt(64): with Q and K stored in bf16 the score
 # error grows with c |q| |k|, past the 1e-2 bar, so that case runs in fp32 only.
 @pytest.mark.parametrize("dtype,c", [("bf16", 0.0), ("bf16", -0.2), ("bf16", 0.3),
