@@ -17,8 +17,9 @@
 // attn_tc_kernel<DQK, DV> (DV = 128, d_vh of 72..128; 384 threads):
 //   warps 0, 2    TMA producers: warp 0 loads the Q tiles of each unit and the
 //                 K blocks, warp 2 the V blocks, into a STAGES-deep ring (K
-//                 and V freed separately); each also prefetches the blocks a
-//                 few steps ahead into L2
+//                 and V freed separately); no requests ahead of the ring
+//                 (L2 prefetches of the blocks past it made every workload
+//                 slower)
 //   warps 1, 3    MMA issuers, one per tile t: S_t = Q_t K_j^T (SMEM x SMEM
 //                 -> TMEM) and z_t += P_t V_j (P from TMEM, V from SMEM); the
 //                 two tiles' streams interleave on the tensor pipe, so one
@@ -78,7 +79,6 @@ constexpr int BLK_N = 128;  // keys per block
 constexpr int NTHREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;  // raise m only when the max grows by > 2^8
-constexpr int PREFETCH = 4;           // K/V blocks requested into L2 ahead of the ring
 
 struct AttnTcParams {
   CUtensorMap qmap;  // Q: dims {d_h, n_q, B*h}, box {64, 128, 1}
@@ -274,8 +274,7 @@ struct Ring {
 // (warp 0), else the V blocks (warp 2), unit after unit through the same
 // STAGES-deep ring (the ring position `it` runs on across units, so the next
 // unit's first blocks load while the current unit's last ones are still
-// being used); each also asks L2 for the blocks PREFETCH ahead so that
-// refills come from L2.
+// being used).
 template <class C, bool SPLIT>
 __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bool is_k,
                                         const WaitCtl& w) {
@@ -324,16 +323,6 @@ __device__ __forceinline__ void produce(const AttnTcParams& P, const Ring& R, bo
       mbar_arrive_expect_tx(&full[s], bytes);
       for (int p = 0; p < panels; ++p)
         tma_load_3d(dst + p * 16384, map, &full[s], 64 * p, (u.kb0 + kb) * BLK_N, bh);
-      // L2 requests for the blocks past the ring, after the first block's
-      // load so that they do not delay it
-      if (kb == 0)
-        for (int pk = C::STAGES; pk < C::STAGES + PREFETCH && pk < u.nmax; ++pk)
-          for (int p = 0; p < panels; ++p)
-            tma_prefetch_l2_3d(map, 64 * p, (u.kb0 + pk) * BLK_N, bh);
-      const int ahead = kb + C::STAGES + PREFETCH;
-      if (ahead < u.nmax)
-        for (int p = 0; p < panels; ++p)
-          tma_prefetch_l2_3d(map, 64 * p, (u.kb0 + ahead) * BLK_N, bh);
     }
     ++ui;
   }

@@ -222,14 +222,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
-// Starts fetching a tile into L2 only (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the fifth-generation MMA
 // ---------------------------------------------------------------------------
