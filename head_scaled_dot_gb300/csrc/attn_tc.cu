@@ -24,11 +24,12 @@
 //                 -> TMEM) and z_t += P_t V_j (P from TMEM, V from SMEM); the
 //                 two tiles' streams interleave on the tensor pipe, so one
 //                 tile's softmax overlaps the other tile's MMAs
-//   warps 4..11   softmax, tile 0 then tile 1 of every key block; a row is
-//                 split over the two warps that see its TMEM lane (64 keys
-//                 each, partial maxima exchanged through shared memory); p is
-//                 written as bf16 over the columns of S (P aliases S), and z / l
-//                 at the end of the unit in the concatenated layout
+//   warps 4..11   softmax, tile 0 then tile 1 of every key block; a warp
+//                 holds 16 rows of its 32-lane TMEM slice, lanes i and i + 16
+//                 the two 64-key halves of one row (half-split TMEM loads),
+//                 so the row maximum and sum take one shuffle; p is written
+//                 as bf16 over the columns of S (P aliases S), and z / l at
+//                 the end of the unit in the concatenated layout
 //
 // attn_tc_sp_kernel<DQK> (d_vh = 64; 640 threads): the same roles, but S, P
 // and z of both tiles have TMEM columns of their own and each tile has its
