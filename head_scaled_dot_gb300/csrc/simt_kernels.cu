@@ -103,22 +103,28 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
 
 constexpr int TA_C = 64;  // keys per block
 
-// 16 bytes from p as floats (zeros when !ok; p is 16-byte aligned when ok).
-__device__ __forceinline__ void load_vec(const float* p, bool ok, float (&v)[4]) {
-  const float4 a = ok ? *reinterpret_cast<const float4*>(p) : make_float4(0.f, 0.f, 0.f, 0.f);
-  v[0] = a.x;
-  v[1] = a.y;
-  v[2] = a.z;
-  v[3] = a.w;
+// 16 bytes from p (zeros when !ok; p is 16-byte aligned when ok).
+__device__ __forceinline__ uint4 load16(const void* p, bool ok) {
+  return ok ? *reinterpret_cast<const uint4*>(p) : make_uint4(0, 0, 0, 0);
 }
-__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, bool ok, float (&v)[8]) {
-  const uint4 a = ok ? *reinterpret_cast<const uint4*>(p) : make_uint4(0, 0, 0, 0);
+// 16 bytes as floats: four fp32 or eight bf16 values.
+__device__ __forceinline__ void unpack16(const uint4& a, float (&v)[4]) {
+  v[0] = __uint_as_float(a.x);
+  v[1] = __uint_as_float(a.y);
+  v[2] = __uint_as_float(a.z);
+  v[3] = __uint_as_float(a.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& a, float (&v)[8]) {
   const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     v[2 * i] = __uint_as_float(w[i] << 16);
     v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
+}
+template <int VEC>
+__device__ __forceinline__ void load_vec(const void* p, bool ok, float (&v)[VEC]) {
+  unpack16(load16(p, ok), v);
 }
 
 struct AttnParams {
@@ -184,12 +190,46 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_consta
     for (int j = 0; j < NV; ++j) z[i][j] = 0.f;
   }
 
-  // 16-byte loads of K and V rows when every row starts on 16 bytes
+  // 16-byte loads of K and V rows when every row starts on 16 bytes. When a
+  // block's K and V are at most 256 vectors each (bf16 heads up to 32, fp32
+  // up to 16), each thread loads its vector of the next block into registers
+  // while the current block is computed and stores it to shared memory at
+  // the top of the next block, so the loads' latency is not waited for.
   constexpr int VEC = 16 / sizeof(T);
   const bool vec = P.vec_kv;
+  const int kvec = dq / VEC, vvec = DVP / VEC;
+  const bool ahead = vec && TA_C * kvec <= 256 && TA_C * vvec <= 256;
+  uint4 kreg = make_uint4(0, 0, 0, 0), vreg = make_uint4(0, 0, 0, 0);
+  auto fetch = [&](int kb) {
+    if (tid < TA_C * kvec) {
+      const int c = tid / kvec, k = (tid % kvec) * VEC;
+      kreg = load16(Kg + (long long)(kb + c) * dq + k, kb + c < L);
+    }
+    if (tid < TA_C * vvec) {
+      const int c = tid / vvec, col = (tid % vvec) * VEC;
+      vreg = load16(Vg + (long long)(kb + c) * dv + col, kb + c < L && col < dv);
+    }
+  };
+  if (ahead && k_end > 0) fetch(0);
   for (int k0 = 0; k0 < k_end; k0 += TA_C) {
     __syncthreads();  // the previous block's K, V and P are no longer read
-    if (vec) {
+    if (ahead) {
+      if (tid < TA_C * kvec) {
+        const int c = tid / kvec, k = (tid % kvec) * VEC;
+        float v[VEC];
+        unpack16(kreg, v);
+#pragma unroll
+        for (int u = 0; u < VEC; ++u) Ks[(k + u) * TA_C + c] = v[u];
+      }
+      if (tid < TA_C * vvec) {
+        const int c = tid / vvec, col = (tid % vvec) * VEC;
+        float v[VEC];
+        unpack16(vreg, v);
+#pragma unroll
+        for (int u = 0; u < VEC; ++u) Vs[c * DVP + col + u] = v[u];
+      }
+      if (k0 + TA_C < k_end) fetch(k0 + TA_C);
+    } else if (vec) {
       for (int e = tid; e < TA_C * (dq / VEC); e += 256) {
         const int c = e / (dq / VEC), k = (e % (dq / VEC)) * VEC;
         float v[VEC];
