@@ -146,7 +146,7 @@ struct AttnParams {
 // row's running summary (m, l, z), in base 2 (scores pre-multiplied by
 // c log2(e)). Thread (ty, tx) holds the scores of rows RT ty + i and keys
 // 4 tx + j (i < RT, j < 4), its share of each row's sum l, and z of rows
-// RT ty + i, columns tx + 16 j (j < NV; d_vh <= 16 NV). The row maximum of a
+// RT ty + i, columns NV tx + j (j < NV; d_vh <= 16 NV). The row maximum of a
 // block is taken across the 16 threads of a row (shuffles within a half
 // warp); P goes through shared memory for z += P V. Register tiles keep a
 // dozen or more FMAs per shared-memory load.
@@ -329,12 +329,29 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_consta
         pa[i4 + 2] = pv.z;
         pa[i4 + 3] = pv.w;
       }
+      // this thread's NV adjacent columns of V row c, in one to four loads
+      float va[NV];
+      const float* vrow = Vs + c * DVP + NV * tx;
+      if constexpr (NV == 1) {
+        va[0] = vrow[0];
+      } else if constexpr (NV == 2) {
+        const float2 t2 = *reinterpret_cast<const float2*>(vrow);
+        va[0] = t2.x;
+        va[1] = t2.y;
+      } else {
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const float v = Vs[c * DVP + tx + 16 * j];
-#pragma unroll
-        for (int i = 0; i < RT; ++i) z[i][j] = fmaf(pa[i], v, z[i][j]);
+        for (int j4 = 0; j4 < NV; j4 += 4) {
+          const float4 t4 = *reinterpret_cast<const float4*>(vrow + j4);
+          va[j4] = t4.x;
+          va[j4 + 1] = t4.y;
+          va[j4 + 2] = t4.z;
+          va[j4 + 3] = t4.w;
+        }
       }
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+#pragma unroll
+        for (int i = 0; i < RT; ++i) z[i][j] = fmaf(pa[i], va[j], z[i][j]);
     }
   }
   // the row sum is spread over the row's 16 threads
@@ -351,7 +368,7 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(const __grid_consta
     T* zrow = Zg + ((long long)b * P.n_q + q) * (long long)P.h * dv + (long long)head * dv;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const int col = tx + 16 * j;
+      const int col = NV * tx + j;
       if (col < dv) zrow[col] = from_f<T>(computed ? z[i][j] * inv : 0.f);
     }
   }
