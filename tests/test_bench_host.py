@@ -59,3 +59,28 @@ def test_reference_arm_prints_one_json_line():
     for k, v in bench.workload_config(w, lens).items():
         assert d["config"][k] == v, k
     assert d["metric"] == bench.METRIC and d["higher_is_better"] is True
+
+
+def test_stored_traffic_entries_name_existing_sources_and_profiles():
+    """profiles/traffic.json (the per-launch DRAM bytes the benchmark line
+    reports beside its roofline) names, for every entry, a kernel source of
+    the package, its hash and the committed ncu summary the bytes come from;
+    the bench looks an entry up only while the hash matches the source."""
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        table = json.load(f)
+    assert set(table) <= {"attention", "qkv_projection", "output_projection"}
+    for kernel, entries in table.items():
+        for workload, e in entries.items():
+            src = os.path.join(ROOT, "head_scaled_dot_gb300", "csrc", e["source"])
+            assert os.path.exists(src), (kernel, workload)
+            assert len(e["source_sha256_16"]) == 16
+            assert isinstance(e["dram_bytes_per_launch"], int) and e["dram_bytes_per_launch"] > 0
+            summary = e["from"].split("profiles/")[-1]
+            assert os.path.exists(os.path.join(ROOT, "profiles", summary)), summary
+            got = bench.stored_traffic(kernel, workload)
+            if bench.source_hash(src) == e["source_sha256_16"]:
+                assert got == e["dram_bytes_per_launch"]
+            else:
+                assert got is None
