@@ -101,6 +101,34 @@ def test_forced_split_all_masks(d, mask, nsplit):
     assert rel_err(got, ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("d", [(128, 128), (64, 128), (96, 72)])
+@pytest.mark.parametrize("shape", [(128, 1000, "none", False), (1, 777, "padding", False),
+                                   (64, 3000, "padding", False), (120, 120, "causal", True),
+                                   (100, 100, "causal_padding", True)],
+                         ids=lambda s: "%dx%d_%s" % s[:3])
+@pytest.mark.parametrize("nsplit", [0, 2, 5])
+def test_single_tile_split(d, shape, nsplit):
+    """At most 128 query rows with the keys split: every unit holds a single
+    query tile (the second tile of each pair has no rows), for both attention
+    kernels' head sizes and the masks of self- and cross-attention."""
+    d_h, d_vh = d
+    n_q, n_k, mask, self_attention = shape
+    B, h = 2, 3
+    Q, K, V = draw(B, h, n_q, n_k, d_h, d_vh, 7 * nsplit + d_h + n_q)
+    lens = [n_k, max(1, n_k // 3)] if "padding" in mask else None
+    c = 1 / math.sqrt(d_h)
+    Z = mha.attention_split(Q.cuda(), K.cuda(), V.cuda(), c, mask, lens,
+                            self_attention=self_attention, nsplit=nsplit)
+    torch.cuda.synchronize()
+    got = f64(Z)
+    ref = oracle_z(Q, K, V, c, mask, lens, self_attention)
+    assert np.isfinite(got).all()
+    if lens is not None and self_attention:
+        for b, L in enumerate(lens):
+            assert np.all(got[b, L:] == 0.0), "padded query rows must be exactly zero"
+    assert rel_err(got, ref) <= TOL["bf16"]
+
+
 def test_workload_one_shape_split_in_two():
     """The B=4, T=1024, h=12, d=64 workload's attention step with its keys cut
     in two ranges: every element against the oracle."""
