@@ -504,7 +504,9 @@ def measure_decode(w, steps, warmup, dev, pk):
     return {"ms_per_launch": ms, "bytes_per_launch": nbytes,
             "roofline": {"kernel": "decode (split summaries + merge)", "bound": "hbm",
                          "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"]},
+                         "frac": gbs / pk["hbm_gbs"],
+                         # DRAM bytes of the streaming kernel (the call's dominant one)
+                         "traffic": stored_traffic("decode", w.name)},
             "config": {"B": w.B, "h": w.h, "n_q": w.n_q, "n_k": w.n_k, "d_h": w.d_h,
                        "d_vh": w.d_vh, "cache_len": lens, "causal_tail": w.causal_tail}}
 

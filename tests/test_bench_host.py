@@ -70,7 +70,7 @@ def test_stored_traffic_entries_name_existing_sources_and_profiles():
     import bench
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         table = json.load(f)
-    assert set(table) <= {"attention", "qkv_projection", "output_projection"}
+    assert set(table) <= {"attention", "qkv_projection", "output_projection", "decode"}
     for kernel, entries in table.items():
         for workload, e in entries.items():
             src = os.path.join(ROOT, "head_scaled_dot_gb300", "csrc", e["source"])
