@@ -76,7 +76,7 @@ extern "C" {
 typedef enum {
   MHA_OK = 0,
   MHA_ERR_INVALID_ARG = 1,    /* a NULL or non-positive argument, a bad enum, non-finite c */
-  MHA_ERR_UNSUPPORTED = 2,    /* a valid shape this build does not handle (see mha_forward) */
+  MHA_ERR_UNSUPPORTED = 2,    /* a valid shape the library does not handle (see mha_forward) */
   MHA_ERR_EMPTY_ROW = 3,      /* some query row would have no allowed key */
   MHA_ERR_WORKSPACE = 4,      /* workspace NULL, misaligned or smaller than mha_workspace_size */
   MHA_ERR_CUDA = 5,           /* a CUDA runtime call or a launch failed */
