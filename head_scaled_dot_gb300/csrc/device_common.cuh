@@ -85,46 +85,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// As mbar_try_wait, without acquire ordering. For the thread that issues
-// tcgen05.mma: there an acquire wait costs the tensor pipe a couple of hundred
-// cycles (it orders behind the thread's MMAs still in flight), a relaxed one
-// nothing.
-__device__ __forceinline__ bool mbar_try_wait_relaxed(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait with mbar_try_wait_relaxed (see there), for the MMA-issuing
-// thread. What it waits for is complete when the phase completes: TMA data
-// (complete_tx) or tensor-memory writes that the writers finished
-// (tcgen05.wait::st, tcgen05.fence::before_thread_sync) before arriving; the
-// caller issues its MMAs only after the wait returns, behind
-// tcgen05.fence::after_thread_sync.
-static __device__ __forceinline__ bool mbar_wait_relaxed(uint64_t* bar, uint32_t parity,
-                                                         const WaitCtl& w) {
-  if (mbar_try_wait_relaxed(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1; it != 0; ++it) {
-    if (mbar_try_wait_relaxed(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*w.abort) return false;
-      if (globaltimer_ns() - t0 > w.limit_ns) {
-        report_error(w, MHA_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
-    }
-  }
-  report_error(w, MHA_ERR_DEVICE_TIMEOUT);
-  return false;
-}
-
 // Waits until the barrier phase with the given parity has completed. Returns
 // false (and records MHA_ERR_DEVICE_TIMEOUT) after w.limit_ns, or at once when
 // another role of the CTA has already given up. Never spins without bound:
@@ -150,25 +110,6 @@ static __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t pa
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, w);
-}
-
-// Waits until the shared-memory counter reaches `target` (a monotonic count
-// written by another thread of the CTA). Bounded like mbar_wait.
-static __device__ __forceinline__ bool counter_wait(volatile int* ctr, int target, const WaitCtl& w) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1; it != 0; ++it) {
-    if (*ctr >= target) return true;
-    if ((it & 31u) == 0) {
-      if (*w.abort) return false;
-      if (globaltimer_ns() - t0 > w.limit_ns) {
-        report_error(w, MHA_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
-    }
-    __nanosleep(32);
-  }
-  report_error(w, MHA_ERR_DEVICE_TIMEOUT);
-  return false;
 }
 
 // ---------------------------------------------------------------------------
@@ -397,39 +338,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
 // Half-split shape 16x32bx2: the warp reads 16 TMEM lanes (the lane field of
 // taddr is the first); thread i < 16 gets lane i's columns [0, N) from taddr's
 // column, thread i + 16 lane i's columns [OFF, OFF + N). A row can thus be
@@ -517,18 +425,6 @@ __device__ __forceinline__ void grid_dep_wait() {
 
 __device__ __forceinline__ void grid_dep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
-
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "elect.sync _|P, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, P;\n\t}\n"
-      : "=r"(pred));
-  return pred != 0;
 }
 
 }  // namespace mha
